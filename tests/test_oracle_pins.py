@@ -1,0 +1,256 @@
+"""Pins for the CPU oracle: every check here is independent of the oracle's
+own code (closed forms, a hand-derived worked example, library routines,
+finite differences, identities the pages state), chosen so that a dropped
+term, a wrong sign, a wrong index or a transposed operand in the oracle fails
+at least one of them.  CPU only.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from online_softmax_05_gb300.inputs import make_inputs, to_f64
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --- online softmax ("Lab 06", section 2) ----------------------------------
+
+@pytest.mark.parametrize("block", [1, 7, 11, 16, 32, 1000, 5000])
+def test_online_softmax_matches_logsumexp(block):
+    x = rng(1).normal(size=1000) * 5.0
+    m, l = oracle.online_softmax_stats(x, block)
+    assert m == np.max(x)
+    assert abs((m + math.log(l)) - scipy.special.logsumexp(x)) < 1e-12
+
+
+@pytest.mark.parametrize("block", [1, 3, 7, 16])
+def test_online_softmax_growing_max(block):
+    # the running max jumps from -40 to 1000 part-way through the row
+    x = np.concatenate([np.full(20, -40.0), rng(2).normal(size=13), [1000.0], rng(3).normal(size=9)])
+    m, l = oracle.online_softmax_stats(x, block)
+    assert np.isfinite(l) and l >= 1.0
+    assert m == 1000.0
+    assert abs((m + math.log(l)) - scipy.special.logsumexp(x)) < 1e-12
+
+
+def test_online_softmax_two_pass_equivalence():
+    # online (m, l) equals the two-pass result: max first, then sum of exp
+    x = rng(4).normal(size=257) * 30.0
+    m2 = np.max(x)
+    l2 = np.sum(np.exp(x - m2))
+    for block in (7, 11, 16, 32):
+        m, l = oracle.online_softmax_stats(x, block)
+        assert m == m2
+        assert abs(l - l2) <= 1e-12 * l2
+
+
+# --- hand-derived worked example (tests/golden/two_key_closed_form.json) ---
+
+def test_two_key_closed_form():
+    with open(os.path.join(GOLDEN, "two_key_closed_form.json")) as f:
+        fx = json.load(f)
+    for c in fx["cases"]:
+        q, k, v, do = (np.array(c[n]) for n in ("q", "k", "v", "do"))
+        o, lse = oracle.attn_fwd(q[None], k[None], v[None], c["scale"], c["causal"])
+        np.testing.assert_allclose(o[0], c["o"], rtol=0, atol=1e-14, err_msg=c["name"])
+        np.testing.assert_allclose(lse[0], c["lse"], rtol=0, atol=1e-14, err_msg=c["name"])
+        dq, dk, dv, dvec = oracle.attn_bwd(q[None], k[None], v[None], do[None], c["scale"], c["causal"])
+        np.testing.assert_allclose(dq[0], c["dq"], rtol=0, atol=1e-14, err_msg=c["name"])
+        np.testing.assert_allclose(dk[0], c["dk"], rtol=0, atol=1e-14, err_msg=c["name"])
+        np.testing.assert_allclose(dv[0], c["dv"], rtol=0, atol=1e-14, err_msg=c["name"])
+        np.testing.assert_allclose(dvec[0], c["dvec"], rtol=0, atol=1e-14, err_msg=c["name"])
+
+
+# --- forward ---------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probs_rows_sum_to_one_and_mask(causal):
+    T, D = 53, 8
+    q, k = rng(5).normal(size=(T, D)), rng(6).normal(size=(T, D))
+    P = oracle.attn_probs(q, k, 0.7, causal)
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert (P >= 0).all()
+    if causal:
+        assert (P[np.triu_indices(T, 1)] == 0.0).all()
+        assert (P[np.tril_indices(T)] > 0.0).all()
+    else:
+        assert (P > 0).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("scale", [0.125, 1.0, -0.3])
+def test_lse_matches_direct_logsumexp(causal, scale):
+    # LSE_i = log sum_j exp(scale q_i.k_j) over visible j, by numpy matmul + scipy logsumexp
+    T, D = 41, 16
+    q, k, v = (rng(s).normal(size=(2, T, D)) for s in (7, 8, 9))
+    o, lse = oracle.attn_fwd(q, k, v, scale, causal)
+    for h in range(2):
+        S = scale * (q[h] @ k[h].T)
+        if causal:
+            S = np.where(np.tril(np.ones((T, T), bool)), S, -np.inf)
+        np.testing.assert_allclose(lse[h], scipy.special.logsumexp(S, axis=1), rtol=0, atol=1e-12)
+        P = scipy.special.softmax(S, axis=1)
+        np.testing.assert_allclose(o[h], P @ v[h], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_uniform_scores_give_mean_of_visible_v(causal):
+    # Q = 0: every visible score is 0, so O_i = mean of V over visible keys, LSE_i = log(#visible)
+    T, D = 37, 5
+    q = np.zeros((T, D))
+    k, v = rng(10).normal(size=(T, D)), rng(11).normal(size=(T, D))
+    o, lse = oracle.attn_fwd(q[None], k[None], v[None], 0.5, causal)
+    for i in range(T):
+        n = i + 1 if causal else T
+        np.testing.assert_allclose(o[0, i], v[:n].mean(axis=0), rtol=0, atol=1e-13)
+        assert abs(lse[0, i] - math.log(n)) < 1e-13
+
+
+def test_causal_row_zero_returns_v0():
+    T, D = 19, 7
+    q, k, v = (rng(s).normal(size=(T, D)) * 3 for s in (12, 13, 14))
+    o, lse = oracle.attn_fwd(q[None], k[None], v[None], 0.4, True)
+    np.testing.assert_array_equal(o[0, 0], v[0])
+    assert abs(lse[0, 0] - 0.4 * float(q[0] @ k[0])) < 1e-13
+
+
+def test_permuting_keys_noncausal_is_invariant():
+    # non-causal attention is invariant under a joint permutation of K and V rows
+    T, D = 29, 6
+    q, k, v = (rng(s).normal(size=(T, D)) for s in (15, 16, 17))
+    perm = rng(18).permutation(T)
+    o1, l1 = oracle.attn_fwd(q[None], k[None], v[None], 0.9, False)
+    o2, l2 = oracle.attn_fwd(q[None], k[perm][None], v[perm][None], 0.9, False)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("T,bq,bk", [(33, 7, 11), (37, 16, 32), (64, 32, 16), (40, 7, 7), (1, 7, 11), (100, 11, 7)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiled_recurrence_equals_naive(T, bq, bk, causal):
+    # the tiled (m, l, acc) recurrence with block sizes that do not divide T equals the definition
+    D = 8
+    q, k, v = (rng(s).normal(size=(T, D)) * 2 for s in (19, 20, 21))
+    o1, l1 = oracle.attn_fwd(q[None], k[None], v[None], 0.6, causal)
+    o2, l2 = oracle.flash_fwd_tiled(q, k, v, 0.6, causal, bq, bk)
+    np.testing.assert_allclose(o2, o1[0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1[0], rtol=0, atol=1e-12)
+
+
+def test_tiled_recurrence_large_logits():
+    # the max grows by hundreds between key tiles: the rescale must stay exact and finite
+    T, D = 48, 4
+    q = rng(22).normal(size=(T, D))
+    k = rng(23).normal(size=(T, D)) * np.linspace(0.1, 200, T)[:, None]
+    v = rng(24).normal(size=(T, D))
+    o1, l1 = oracle.attn_fwd(q[None], k[None], v[None], 1.0, False)
+    o2, l2 = oracle.flash_fwd_tiled(q, k, v, 1.0, False, 8, 8)
+    assert np.isfinite(o2).all() and np.isfinite(l2).all()
+    np.testing.assert_allclose(o2, o1[0], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(l2, l1[0], rtol=1e-13, atol=0)
+
+
+def test_rows_variant_matches_full():
+    T, D = 70, 8
+    q, k, v = (rng(s).normal(size=(T, D)) for s in (25, 26, 27))
+    rows = [0, 1, 17, 69]
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q[None], k[None], v[None], 0.3, causal)
+        o_r, l_r = oracle.attn_fwd_rows(q, k, v, 0.3, causal, rows)
+        np.testing.assert_array_equal(o_r, o[0, rows])
+        np.testing.assert_array_equal(l_r, lse[0, rows])
+
+
+# --- backward ("Lab 06", section 4) ----------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rowsum_identity(causal):
+    # D_i = sum_j P_ij dP_ij (oracle, by definition) equals rowsum(dO o O)
+    T, D = 45, 12
+    q, k, v, do = (rng(s).normal(size=(2, T, D)) for s in (28, 29, 30, 31))
+    o, _ = oracle.attn_fwd(q, k, v, 0.25, causal)
+    _, _, _, dvec = oracle.attn_bwd(q, k, v, do, 0.25, causal)
+    np.testing.assert_allclose(dvec, (do * o).sum(axis=-1), rtol=0, atol=1e-10)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("T,D", [(1, 3), (5, 2), (9, 4)])
+def test_finite_difference_gradients(causal, T, D):
+    # L = sum(dO o O); central differences with h = 1e-6, relative error < 1e-6
+    q, k, v, do = (rng(s).normal(size=(1, T, D)) for s in (32, 33, 34, 35))
+    scale = 0.8
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, scale, causal)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attn_fwd(qq, kk, vv, scale, causal)
+        return float((o * do).sum())
+
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = {"q": q, "k": k, "v": v}
+            args_p[name], args_m[name] = xp, xm
+            fd[idx] = (loss(**{"qq": args_p["q"], "kk": args_p["k"], "vv": args_p["v"]})
+                       - loss(**{"qq": args_m["q"], "kk": args_m["k"], "vv": args_m["v"]})) / (2 * h)
+        denom = max(np.abs(g).max(), 1e-3)
+        assert np.abs(fd - g).max() / denom < 1e-6, name
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_torch_autograd_float64(causal):
+    # the analytic gradients equal autograd through softmax(QK^T scale) V in float64
+    T, D = 37, 16
+    q, k, v, do = (torch.from_numpy(rng(s).normal(size=(3, T, D))) for s in (36, 37, 38, 39))
+    scale = 0.25
+    qt, kt, vt = (x.clone().requires_grad_(True) for x in (q, k, v))
+    S = scale * qt @ kt.transpose(-1, -2)
+    if causal:
+        S = S.masked_fill(~torch.ones(T, T, dtype=torch.bool).tril(), float("-inf"))
+    O = torch.softmax(S, dim=-1) @ vt
+    O.backward(do)
+    dq, dk, dv, _ = oracle.attn_bwd(q.numpy(), k.numpy(), v.numpy(), do.numpy(), scale, causal)
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(oracle.attn_fwd(q.numpy(), k.numpy(), v.numpy(), scale, causal)[0],
+                               O.detach().numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_rows_variant_matches_full(causal):
+    T, D = 66, 8
+    q, k, v, do = (rng(s).normal(size=(T, D)) for s in (40, 41, 42, 43))
+    dq, dk, dv, dvec = oracle.attn_bwd(q[None], k[None], v[None], do[None], 0.35, causal)
+    _, lse = oracle.attn_fwd(q[None], k[None], v[None], 0.35, causal)
+    rq, rk = [0, 5, 64, 65], [0, 1, 33, 65]
+    dq_r, dk_r, dv_r, lse_r, dvec_r = oracle.attn_bwd_rows(q, k, v, do, 0.35, causal, rq, rk)
+    np.testing.assert_allclose(dq_r, dq[0, rq], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk_r, dk[0, rk], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv_r, dv[0, rk], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse_r, lse[0], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dvec_r, dvec[0], rtol=0, atol=1e-12)
+
+
+def test_oracle_on_generated_bf16_inputs_is_finite():
+    # the seeded bf16 inputs of the large-logit recipe stay finite through the oracle
+    q, k, v, do = make_inputs(1, 2, 64, 16, seed=0, qk_std=4.0, big_row_frac=0.05, big_row_mult=10.0)
+    q, k, v, do = (to_f64(t) for t in (q, k, v, do))
+    o, lse = oracle.attn_fwd(q, k, v, 0.25, False)
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, 0.25, False)
+    for a in (o, lse, dq, dk, dv):
+        assert np.isfinite(a).all()
