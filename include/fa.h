@@ -1,0 +1,136 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * What it computes (pages: "Lab 06 - Attention kernels: online softmax ->
+ * FlashAttention -> Triton", sections 3 and 4; "Triton FlashAttention-2
+ * forward", section "The kernel"; "Flash Attention and Kernel Optimization",
+ * sections "Running softmax state", "Causal masking", "Output and saved
+ * state"):
+ *
+ *   forward   S = Q K^T * scale, key j visible to query i iff j <= i when
+ *             causal; O = softmax(S) V; LSE_i = log sum_j exp(S_ij)
+ *             (natural log of the scaled scores), computed tile by tile
+ *             with the online-softmax recurrence, never forming S in memory.
+ *   backward  D_i = rowsum(dO o O); P = exp(S - LSE) recomputed per tile;
+ *             dV = P^T dO; dP = dO V^T; dS = P o (dP - D);
+ *             dQ = dS K * scale; dK = dS^T Q * scale.
+ *
+ * Layout.  Every tensor is contiguous (B, H, T, D) in bf16
+ * (__nv_bfloat16, passed as void*), row stride D elements, head stride T*D.
+ * LSE is contiguous (B, H, T) float32.  D must be 64 or 128.  T_q = T_k = T.
+ *
+ * Memory and ownership.  All tensor pointers are DEVICE pointers on the
+ * current CUDA device, allocated and owned by the caller; the library keeps
+ * no pointer after a call returns.  Base pointers must be 16-byte aligned
+ * (the kernels move tiles with TMA).  Outputs must not overlap inputs.
+ *
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream).  Calls are asynchronous: they enqueue kernels on `stream` and
+ * return without synchronising.  fa_bwd takes its workspace (B*H*T floats for
+ * D, B*H*T*D floats for the dQ accumulator, B*H*T_pad floats for log2-scaled
+ * LSE) stream-ordered with cudaMallocAsync on `stream` and releases it with
+ * cudaFreeAsync on the same stream before returning.
+ *
+ * Errors.  Every entry point validates its arguments before launching
+ * anything; on a validation error nothing is enqueued.  Return value 0
+ * (FA_OK) or a negative fa_status.  A kernel that detects a stalled pipeline
+ * (a bounded wait that ran out) records FA_ERR_DEVICE_TIMEOUT in a device
+ * status word and exits cleanly; read it with fa_get_device_status.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_NULL = -1,            /* a required pointer is NULL */
+    FA_ERR_SHAPE = -2,           /* B, H or T < 1, or a size overflows the index types */
+    FA_ERR_UNSUPPORTED = -3,     /* D is not 64 or 128 */
+    FA_ERR_ALIGN = -4,           /* a base pointer is not 16-byte aligned */
+    FA_ERR_CUDA = -5,            /* a CUDA runtime / driver call failed (launch, attribute, tensor map) */
+    FA_ERR_NOMEM = -6,           /* stream-ordered workspace allocation failed */
+    FA_ERR_DEVICE_TIMEOUT = -7,  /* a kernel's bounded wait ran out (pipeline stall); outputs invalid */
+    FA_ERR_ARG = -8,             /* causal not 0/1, or scale not finite */
+    FA_ERR_ARCH = -9             /* current device is not compute capability 10.3 (sm_103a) */
+} fa_status;
+
+/*
+ * Forward pass.
+ *   q, k, v  in : (B, H, T, D) bf16
+ *   o        out: (B, H, T, D) bf16, O = softmax(Q K^T scale [+ causal mask]) V
+ *   lse      out: (B, H, T) float32, natural-log log-sum-exp of the scaled,
+ *                 masked scores of each row (the only statistic the backward
+ *                 needs: "Lab 06", section 4 and "Check yourself" item 3)
+ *   scale       : finite float multiplying Q K^T (usually 1/sqrt(D))
+ *   causal      : 0 = full attention, 1 = key j visible to query i iff j <= i
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int T, int D, float scale, int causal, void* stream);
+
+/*
+ * Backward pass.
+ *   q, k, v, o, dO in : (B, H, T, D) bf16 (o from fa_fwd on the same inputs)
+ *   lse            in : (B, H, T) float32 from fa_fwd
+ *   dq, dk, dv     out: (B, H, T, D) bf16 gradients of sum(dO o O) with
+ *                       respect to q, k, v (overwritten, not accumulated)
+ *   B, H, T, D, scale, causal: as in fa_fwd.
+ * dq is accumulated in float32 across key tiles and rounded to bf16 once.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv,
+           int B, int H, int T, int D, float scale, int causal, void* stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* fa_strerror(int status);
+
+/*
+ * Synchronises `stream`, returns the device status word recorded by the
+ * library's kernels on the current device since the last call (FA_OK or
+ * FA_ERR_DEVICE_TIMEOUT), and clears it.  Returns FA_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+int fa_get_device_status(void* stream);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+/*
+ * Host-only schedule queries (no GPU needed).  They evaluate the exact index
+ * logic the kernels use, so tests can compare it with a brute-force mask.
+ *
+ * fa_sched_fwd_tile_class / fa_sched_bwd_tile_class: class of the tile pair
+ *   (query tile qt, key tile kt) as the forward / backward kernel sees it:
+ *   0 = skipped (never loaded), 1 = full (no element mask), 2 = masked
+ *   element by element.  The backward's query tile height depends on D.
+ * fa_sched_fwd_keep / fa_sched_bwd_keep: 1 iff the kernel's composition of
+ *   tile loop bounds, tile class and element mask keeps score (i, j).
+ *   i and j may range over the padded extent (multiples of the tile sizes).
+ * fa_sched_tile_rows: query tile height (fwd) or key tile height (bwd keys)
+ *   and backward query tile height for head size D: writes bm_fwd, bn, bm_bwd.
+ * Return negative fa_status on bad arguments.
+ */
+int fa_sched_fwd_tile_class(int T, int causal, int qt, int kt);
+int fa_sched_bwd_tile_class(int T, int D, int causal, int qt, int kt);
+int fa_sched_fwd_keep(int T, int causal, int i, int j);
+int fa_sched_bwd_keep(int T, int D, int causal, int i, int j);
+int fa_sched_tile_rows(int D, int* bm_fwd, int* bn, int* bm_bwd);
+
+/*
+ * Test hooks (host state, read at the next launch; default off).
+ * fa_debug_set_wait_timeout_ns: bound of every in-kernel wait (default 2 s).
+ * fa_debug_inject: 0 = off; 1 = the forward's load warp skips its first
+ *   K/V tile copy, so the kernel's bounded waits run out and it reports
+ *   FA_ERR_DEVICE_TIMEOUT instead of hanging.  Used to test failure
+ *   detection without faulting the GPU.
+ */
+int fa_debug_set_wait_timeout_ns(unsigned long long ns);
+int fa_debug_inject(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,156 @@
+"""GB300 (sm_103a) exact attention with the online-softmax recurrence.
+
+A thin ctypes binding over ``libfa.so`` (declared in ``include/fa.h``).  It
+only marshals arguments: every step of the forward and backward pass runs in
+the library's CUDA kernels.  PyTorch is used for device memory and streams.
+There is no CPU fallback: if the library is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = ["fa_fwd", "fa_bwd", "fa_strerror", "fa_get_device_status", "fa_version",
+           "attention_forward", "attention_backward", "FAError", "library_path", "load_library"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libfa.so")
+_lib = None
+_lock = threading.Lock()
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_SHAPE", -3: "FA_ERR_UNSUPPORTED", -4: "FA_ERR_ALIGN",
+                -5: "FA_ERR_CUDA", -6: "FA_ERR_NOMEM", -7: "FA_ERR_DEVICE_TIMEOUT", -8: "FA_ERR_ARG",
+                -9: "FA_ERR_ARCH"}
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({fa_strerror(code)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libfa.so (built in-tree by ``online_softmax_05_gb300.build``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is not built; run `python -m online_softmax_05_gb300.build` "
+                               "(or __graft_entry__.build()) first. There is no CPU fallback.")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.fa_fwd.restype = i
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.fa_bwd.restype = i
+        lib.fa_strerror.argtypes = [i]
+        lib.fa_strerror.restype = ctypes.c_char_p
+        lib.fa_get_device_status.argtypes = [vp]
+        lib.fa_get_device_status.restype = i
+        lib.fa_version.restype = i
+        for name in ("fa_sched_fwd_tile_class", "fa_sched_fwd_keep"):
+            getattr(lib, name).argtypes = [i, i, i, i]
+            getattr(lib, name).restype = i
+        for name in ("fa_sched_bwd_tile_class", "fa_sched_bwd_keep"):
+            getattr(lib, name).argtypes = [i, i, i, i, i]
+            getattr(lib, name).restype = i
+        lib.fa_sched_tile_rows.argtypes = [i, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i)]
+        lib.fa_sched_tile_rows.restype = i
+        lib.fa_debug_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        lib.fa_debug_set_wait_timeout_ns.restype = i
+        lib.fa_debug_inject.argtypes = [i]
+        lib.fa_debug_inject.restype = i
+        _lib = lib
+        return lib
+
+
+def _ptr(x) -> int | None:
+    """Device pointer of a torch tensor, or an int / None passed through."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def fa_fwd(q, k, v, o, lse, B: int, H: int, T: int, D: int, scale: float, causal: int, stream=None) -> int:
+    """C-ABI ``fa_fwd``; tensors (or raw device pointers) in, status code out."""
+    return load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, T, D, float(scale),
+                                 int(causal), _stream(stream))
+
+
+def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B: int, H: int, T: int, D: int, scale: float, causal: int,
+           stream=None) -> int:
+    """C-ABI ``fa_bwd``; tensors (or raw device pointers) in, status code out."""
+    return load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, H, T, D, float(scale), int(causal), _stream(stream))
+
+
+def fa_strerror(code: int) -> str:
+    return load_library().fa_strerror(int(code)).decode()
+
+
+def fa_get_device_status(stream=None) -> int:
+    return load_library().fa_get_device_status(_stream(stream))
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+def _check(t, name):
+    import torch
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
+        raise ValueError(f"{name} must be a contiguous (B, H, T, D) bf16 CUDA tensor")
+
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """O, LSE for contiguous (B, H, T, D) bf16 CUDA tensors (outputs allocated if not given)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    B, H, T, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, T), device=q.device, dtype=torch.float32) if lse is None else lse
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_fwd(q, k, v, out, lse, B, H, T, D, scale, int(causal), stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd")
+    return out, lse
+
+
+def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, dq=None, dk=None,
+                       dv=None, stream=None):
+    """dQ, dK, dV for contiguous (B, H, T, D) bf16 CUDA tensors."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _check(t, n)
+    B, H, T, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, T, D, scale, int(causal), stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd")
+    return dq, dk, dv

@@ -1,0 +1,95 @@
+"""Build the CUDA libraries in-tree with nvcc for sm_103a.
+
+  libfa.so        the product: C-ABI entry points of include/fa.h
+  libfa_probe.so  test-only bring-up kernels (descriptor / TMA checks)
+
+Translation units compile in parallel; a unit is rebuilt only when its
+source or any header under csrc/ or include/ is newer than its object.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import glob
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+
+LIB = os.path.join(PKG, "libfa.so")
+PROBE_LIB = os.path.join(PKG, "libfa_probe.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+                     f"-I{INCLUDE}", f"-I{CSRC}", "--expt-relaxed-constexpr"]
+
+PRODUCT_UNITS = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu"]
+PROBE_UNITS = ["fa_probe.cu"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libfa.so")
+
+
+def _headers_mtime() -> float:
+    hs = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
+        glob.glob(os.path.join(INCLUDE, "*.h"))
+    return max((os.path.getmtime(h) for h in hs), default=0.0)
+
+
+def _compile(unit: str, extra: list[str], force: bool, verbose: bool) -> str:
+    src = os.path.join(CSRC, unit)
+    obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
+    if (not force and os.path.exists(obj)
+            and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime())):
+        return obj
+    cmd = [nvcc()] + NVCC_FLAGS + extra + ["-c", src, "-o", obj + ".tmp"]
+    if verbose:
+        print(" ".join(cmd), flush=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {unit}:\n{r.stdout}\n{r.stderr}")
+    if verbose and (r.stdout or r.stderr):
+        print(r.stdout + r.stderr, flush=True)
+    os.replace(obj + ".tmp", obj)
+    return obj
+
+
+def _link(objs: list[str], out: str, verbose: bool) -> None:
+    newest = max(os.path.getmtime(o) for o in objs)
+    if os.path.exists(out) and os.path.getmtime(out) >= newest:
+        return
+    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", out + ".tmp"] + objs
+    if verbose:
+        print(" ".join(cmd), flush=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed for {out}:\n{r.stdout}\n{r.stderr}")
+    os.replace(out + ".tmp", out)
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, probes: bool = True) -> str:
+    """Compile every CUDA translation unit and link libfa.so (+ libfa_probe.so)."""
+    os.makedirs(BUILD, exist_ok=True)
+    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    units = PRODUCT_UNITS + (PROBE_UNITS if probes else [])
+    with cf.ThreadPoolExecutor(max_workers=len(units)) as ex:
+        futs = {u: ex.submit(_compile, u, extra, force, verbose or ptxas_verbose) for u in units}
+        objs = {u: f.result() for u, f in futs.items()}
+    _link([objs[u] for u in PRODUCT_UNITS], LIB, verbose)
+    if probes:
+        _link([objs[u] for u in PROBE_UNITS], PROBE_LIB, verbose)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose="-v" in sys.argv, ptxas_verbose="--ptxas" in sys.argv)
+    print(LIB)

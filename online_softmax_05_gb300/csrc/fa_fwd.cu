@@ -1,0 +1,504 @@
+// fa_fwd.cu -- exact attention forward on sm_103a with the online-softmax
+// recurrence ("Lab 06 - Attention kernels", section 3; "Triton
+// FlashAttention-2 forward", section "The kernel"; "Flash Attention and
+// Kernel Optimization", sections "Running softmax state", "Causal masking",
+// "Output and saved state").
+//
+// One persistent CTA per SM walks work items (pair of 128-row query tiles,
+// batch*head).  Warp roles:
+//   warps 0-3  softmax for query tile 0 (one TMEM lane = one query row each)
+//   warps 4-7  softmax for query tile 1
+//   warp 8     TMA producer: Q tiles once per item, K/V tiles into a ring
+//   warp 9     tcgen05 issuer: S = Q K^T into TMEM, O += P V with P in TMEM
+// Per key tile j the softmax warps read S_t(j) from TMEM, update the running
+// max m (log2 domain, scale*log2(e) folded in), rescale O only when m grows
+// by more than 2^8 (exact, see below), write P = exp2(S*c - m) as bf16 back
+// into the same TMEM columns and hand it to the MMA warp.  The two query
+// tiles ping-pong: the softmax of one overlaps the tensor-core work of the
+// other.  Finally O = acc / l goes out through shared memory with a TMA store
+// and LSE = (m + log2 l) * ln 2 is written per row.
+//
+// Deferred rescale: O = acc / l and LSE = m_used + log l hold for ANY
+// reference m_used, since e^{x - m} = e^{m' - m} e^{x - m'} ("Lab 06",
+// section 2, "Why the rescale is exact").  Keeping m_used while the true max
+// exceeds it by at most 8 (log2 units) bounds every P by 2^8, far from
+// overflow in fp32 and bf16.
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_sched.h"
+#include "fa_tmap.h"
+
+namespace fa {
+
+static __device__ int g_status_fwd;
+
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kAtoms = D / 64;             // 128-byte swizzle atoms per row
+    static constexpr int kAtomBytes = 128 * 128;      // one atom column of a 128-row tile
+    static constexpr int kTileBytes = 128 * D * 2;    // one 128 x D bf16 tile
+    static constexpr int kStages = (D == 128) ? 4 : 8;
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] epi[2] mma_done
+    static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + tmem slot, abort flag, alignment slack
+    // TMEM columns (512 allocated): S0, S1 (P aliases their first 64 columns), O0, O1
+    __device__ static constexpr uint32_t kS(int t) { return 128u * t; }
+    __device__ static constexpr uint32_t kO(int t) { return 256u + 128u * t; }
+    static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+};
+
+struct FwdParams {
+    float* lse;
+    int T, BH, n_pairs, n_items;
+    float sl2_eff;  // multiplier applied inside exp2: scale*log2e, or 1 when prescaled
+    float sl2;      // scale * log2(e)
+    int prescale;   // 1 when scale <= 0: scores are multiplied by sl2 before the max
+    unsigned long long timeout_ns;
+    int inject;
+};
+
+struct Ctl {
+    volatile int* abort;
+    unsigned long long timeout_ns;
+};
+
+// Bounded wait: true when the phase completed, false when the CTA aborted
+// (this wait ran out of time, or another role already gave up).
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
+    uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*c.abort) return false;
+        if (globaltimer_ns() - t0 > c.timeout_ns) {
+            *c.abort = 1;
+            atomicCAS(&g_status_fwd, 0, kStatusTimeout);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl c) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, c);
+}
+// Warp-uniform wait: lane 0 polls, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, c);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Item k of this CTA in snake order over items sorted heaviest first
+// (causal: later query pairs see more key tiles).
+__device__ __forceinline__ int item_of(int k, int n_items) {
+    int G = gridDim.x;
+    int w = k * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
+    return w < n_items ? w : -1;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdParams p) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ[2] = {sbase + C::kQOff, sbase + C::kQOff + C::kTileBytes};
+    const uint32_t sKV = sbase + C::kKVOff;
+    const uint32_t bars = sbase + C::kBarOff;
+    auto q_full = [&](int t) { return bars + 8u * t; };
+    auto q_empty = [&](int t) { return bars + 8u * (2 + t); };
+    auto kv_full = [&](int s) { return bars + 8u * (4 + s); };
+    auto kv_empty = [&](int s) { return bars + 8u * (4 + C::kStages + s); };
+    auto s_full = [&](int t) { return bars + 8u * (4 + 2 * C::kStages + t); };
+    auto p_full = [&](int t) { return bars + 8u * (6 + 2 * C::kStages + t); };
+    auto o_full = [&](int t) { return bars + 8u * (8 + 2 * C::kStages + t); };
+    auto epi_bar = [&](int t) { return bars + 8u * (10 + 2 * C::kStages + t); };
+    const uint32_t mma_done = bars + 8u * (12 + 2 * C::kStages);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+    const Ctl ctl{abort_flag, p.timeout_ns};
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = p.T;
+
+    if (tid == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(q_full(t), 1);
+            mbar_init(q_empty(t), 1);
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), 4);
+            mbar_init(o_full(t), 1);
+            mbar_init(epi_bar(t), 4);
+        }
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kv_cnt = 0, q_cnt[2] = {0, 0};
+            uint32_t q_armed[2] = {0, 0};
+            int skipped_fill = -1;  // fill index the test hook dropped
+            const uint64_t pol_kv = l2_policy_evict_last();
+            const uint64_t pol_q = l2_policy_evict_first();
+            bool skip_first = (p.inject == 1);
+            for (int k = 0;; ++k) {
+                int w = item_of(k, p.n_items);
+                if (w < 0) break;
+                const int pair = p.n_pairs - 1 - w / p.BH, bh = w % p.BH;
+                const int t0 = 2 * pair, t1 = t0 + 1;
+                const bool valid1 = t1 * kFwdBM < T;
+                const int n0 = fwd_num_kv_tiles(T, CAUSAL, t0);
+                const int n1 = valid1 ? fwd_num_kv_tiles(T, CAUSAL, t1) : 0;
+                const int nmax = n0 > n1 ? n0 : n1;
+                for (int t = 0; t < 2; ++t) {
+                    if (t == 1 && !valid1) continue;
+                    if (!wait_bar(q_empty(t), (q_cnt[t] & 1) ^ 1, ctl)) goto producer_done;
+                    ++q_cnt[t];
+                    mbar_arrive_expect_tx(q_full(t), C::kTileBytes);
+                    ++q_armed[t];
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_3d_hint(sQ[t] + a * C::kAtomBytes, &tm_q, q_full(t), 64 * a, (t0 + t) * kFwdBM, bh,
+                                         pol_q);
+                }
+                for (int j = 0; j < nmax; ++j) {
+                    for (int kind = 0; kind < 2; ++kind) {
+                        const uint32_t slot = kv_cnt % C::kStages;
+                        if (!wait_bar(kv_empty(slot), ((kv_cnt / C::kStages) & 1) ^ 1, ctl)) goto producer_done;
+                        ++kv_cnt;
+                        if (skip_first) {  // test hook: never deliver this tile
+                            skip_first = false;
+                            skipped_fill = static_cast<int>(kv_cnt - 1);
+                            continue;
+                        }
+                        mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
+                        const CUtensorMap* tm = kind ? &tm_v : &tm_k;
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_load_3d_hint(sKV + slot * C::kTileBytes + a * C::kAtomBytes, tm, kv_full(slot),
+                                             64 * a, j * kBN, bh, pol_kv);
+                    }
+                }
+            }
+        producer_done:
+            // make sure no copy is still landing in shared memory before exit
+            Ctl drain{abort_flag, 100000000ull};
+            volatile int never = 0;
+            drain.abort = &never;
+            // the last kStages fills are the only ones that can still be in flight
+            for (uint32_t f = kv_cnt > C::kStages ? kv_cnt - C::kStages : 0; f < kv_cnt; ++f)
+                if (static_cast<int>(f) != skipped_fill)
+                    wait_bar(kv_full(f % C::kStages), (f / C::kStages) & 1, drain);
+            for (int t = 0; t < 2; ++t)
+                if (q_armed[t]) wait_bar(q_full(t), (q_armed[t] - 1) & 1, drain);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t kv_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
+            auto issue_s = [&](int t, uint32_t slot) {
+                const uint32_t qa = sQ[t], ka = sKV + slot * C::kTileBytes;
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint32_t off = (s >> 2) * C::kAtomBytes + (s & 3) * 32;
+                    mma_ss(tmem + C::kS(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                           C::kIdescS, s > 0);
+                }
+            };
+            auto issue_pv = [&](int t, uint32_t slot, bool acc) {
+                const uint32_t va = sKV + slot * C::kTileBytes;
+#pragma unroll
+                for (int s = 0; s < kBN / 16; ++s)
+                    mma_ts(tmem + C::kO(t), tmem + C::kS(t) + s * 8, sdesc_sw128(va + s * 2048, C::kAtomBytes, 1024),
+                           C::kIdescPV, (acc || s > 0) ? 1u : 0u);
+            };
+            for (int k = 0;; ++k) {
+                int w = item_of(k, p.n_items);
+                if (w < 0) break;
+                const int pair = p.n_pairs - 1 - w / p.BH;
+                const int t0 = 2 * pair, t1 = t0 + 1;
+                const bool valid1 = t1 * kFwdBM < T;
+                const int n0 = fwd_num_kv_tiles(T, CAUSAL, t0);
+                const int n1 = valid1 ? fwd_num_kv_tiles(T, CAUSAL, t1) : 0;
+                const int nmax = n0 > n1 ? n0 : n1;
+                if (!wait_bar(q_full(0), q_cnt[0] & 1, ctl)) goto mma_done_label;
+                ++q_cnt[0];
+                if (valid1) {
+                    if (!wait_bar(q_full(1), q_cnt[1] & 1, ctl)) goto mma_done_label;
+                    ++q_cnt[1];
+                }
+                {
+                    const uint32_t ks = kv_cnt % C::kStages;
+                    if (!wait_bar(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                    ++kv_cnt;
+                    tc_fence_after();
+                    issue_s(0, ks);
+                    mma_commit(s_full(0));
+                    if (n1 > 0) {
+                        issue_s(1, ks);
+                        mma_commit(s_full(1));
+                    }
+                    mma_commit(kv_empty(ks));
+                }
+                for (int j = 0; j < nmax; ++j) {
+                    const uint32_t vs = kv_cnt % C::kStages;
+                    if (!wait_bar(kv_full(vs), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                    ++kv_cnt;
+                    tc_fence_after();
+                    const bool has_next = j + 1 < nmax;
+                    const uint32_t ks = kv_cnt % C::kStages;
+                    bool k_ready = false;
+                    for (int t = 0; t < 2; ++t) {
+                        const int n = t ? n1 : n0;
+                        if (j >= n) continue;
+                        if (!wait_bar(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
+                        ++p_cnt[t];
+                        tc_fence_after();
+                        issue_pv(t, vs, j > 0);
+                        if (j + 1 < n) {
+                            if (!k_ready) {
+                                if (!wait_bar(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            issue_s(t, ks);
+                            mma_commit(s_full(t));
+                        } else {
+                            mma_commit(o_full(t));
+                        }
+                    }
+                    mma_commit(kv_empty(vs));
+                    if (has_next) {
+                        if (!k_ready) {
+                            if (!wait_bar(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                        }
+                        mma_commit(kv_empty(ks));
+                        ++kv_cnt;
+                    }
+                }
+            }
+        mma_done_label:
+            // every MMA issued so far must finish before TMEM is released
+            mma_commit(mma_done);
+            Ctl drain{abort_flag, 100000000ull};
+            volatile int never = 0;
+            drain.abort = &never;
+            wait_bar(mma_done, 0, drain);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax (tile t)
+        const int t = warp >> 2, wq = warp & 3;
+        const int r_local = 32 * wq + lane;
+        const uint32_t lane_base = tmem + ((32u * wq) << 16);
+        const uint32_t tS = lane_base + C::kS(t), tO = lane_base + C::kO(t);
+        uint32_t s_cnt = 0, o_cnt = 0, epi_cnt = 0;
+        const float eff = p.sl2_eff;
+        for (int k = 0;; ++k) {
+            int w = item_of(k, p.n_items);
+            if (w < 0) break;
+            const int pair = p.n_pairs - 1 - w / p.BH, bh = w % p.BH;
+            const int tile = 2 * pair + t;
+            if (tile * kFwdBM >= T) continue;  // tile 1 of the last pair may be empty
+            const int row = tile * kFwdBM + r_local;
+            const int n = fwd_num_kv_tiles(T, CAUSAL, tile);
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < n; ++j) {
+                if (!warp_wait(s_full(t), s_cnt & 1, ctl)) goto softmax_done;
+                ++s_cnt;
+                tc_fence_after();
+                uint32_t sr[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence32(sr + 32 * c);
+                float* s = reinterpret_cast<float*>(sr);
+                if (p.prescale) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) s[c] *= p.sl2;
+                }
+                if (fwd_tile_class(T, CAUSAL, tile, j) == kMasked) {
+                    const int key0 = j * kBN;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (!elem_visible(T, CAUSAL, row, key0 + c)) s[c] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+                const float m_tile = mx * eff;
+                const float m_new = fmaxf(m_used, m_tile);
+                float alpha = 1.f;
+                bool need = false;
+                if (j == 0) {
+                    m_used = m_new;
+                } else if (m_new > m_used + kRescaleThreshold) {
+                    need = true;
+                    alpha = ex2_approx(m_used - m_new);
+                    m_used = m_new;
+                    l *= alpha;
+                }
+                const float neg = -m_used;
+                float lp = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = ex2_approx(fmaf(s[2 * c], eff, neg));
+                    const float p1 = ex2_approx(fmaf(s[2 * c + 1], eff, neg));
+                    lp += p0 + p1;
+                    sr[c] = pack_bf16x2(p0, p1);
+                }
+                l += lp;
+                tmem_st32(tS, sr);
+                tmem_st32(tS + 32, sr + 32);
+                // O already holds PV(j-1) (S(j) was committed after it); rescale it
+                // before PV(j) is issued, only when some row's reference max moved.
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t orr[32];
+                        tmem_ld32(tO + 32 * c, orr);
+                        tmem_ld_wait();
+                        reg_fence32(orr);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        tmem_st32(tO + 32 * c, orr);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(t));
+            }
+            // ---- epilogue: O = acc / l through shared memory and a TMA store; LSE per row
+            if (!warp_wait(o_full(t), o_cnt & 1, ctl)) goto softmax_done;
+            ++o_cnt;
+            tc_fence_after();
+            {
+                const float inv = 1.f / l;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(tO + 32 * c, orr);
+                    tmem_ld_wait();
+                    reg_fence32(orr);
+                    const int col0 = 32 * c;
+                    const uint32_t atom = sQ[t] + (col0 >> 6) * C::kAtomBytes;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint32_t chunk = ((col0 & 63) >> 3) + q4;
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w4[e] = pack_bf16x2(__uint_as_float(orr[8 * q4 + 2 * e]) * inv,
+                                                __uint_as_float(orr[8 * q4 + 2 * e + 1]) * inv);
+                        st_shared_v4(atom + sw128_off(r_local, chunk), w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_bar(t));
+                if (wq == 0 && lane == 0) {
+                    if (wait_bar(epi_bar(t), epi_cnt & 1, ctl)) {
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_store_3d(&tm_o, sQ[t] + a * C::kAtomBytes, 64 * a, tile * kFwdBM, bh);
+                        bulk_commit();
+                        bulk_wait_read0();
+                    }
+                    mbar_arrive(q_empty(t));
+                }
+                ++epi_cnt;
+                if (row < T) p.lse[static_cast<size_t>(bh) * T + row] = (m_used + __log2f(l)) * kLn2;
+            }
+        }
+    softmax_done:;
+        if (wq == 0 && lane == 0) bulk_wait0();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool CAUSAL>
+int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                 const FwdParams& p, int grid, cudaStream_t st) {
+    static bool attr_set = false;
+    auto kern = fa_fwd_kernel<D, CAUSAL>;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmemBytes) !=
+            cudaSuccess)
+            return -5;
+        attr_set = true;
+    }
+    kern<<<grid, kFwdThreads, FwdCfg<D>::kSmemBytes, st>>>(tq, tk, tv, to, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+}  // namespace
+
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int D,
+               float scale, bool causal, cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv, to;
+    if (!make_tmap_bhtd(&tq, q, BH, T, D, 128) || !make_tmap_bhtd(&tk, k, BH, T, D, 128) ||
+        !make_tmap_bhtd(&tv, v, BH, T, D, 128) || !make_tmap_bhtd(&to, o, BH, T, D, 128))
+        return -5;
+    FwdParams p;
+    p.lse = lse;
+    p.T = T;
+    p.BH = BH;
+    p.n_pairs = cdiv(T, 2 * kFwdBM);
+    p.n_items = p.n_pairs * BH;
+    p.sl2 = scale * kLog2e;
+    p.prescale = (p.sl2 > 0.f) ? 0 : 1;
+    p.sl2_eff = p.prescale ? 1.f : p.sl2;
+    p.timeout_ns = dbg.timeout_ns;
+    p.inject = dbg.inject;
+    const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+    if (D == 64)
+        return causal ? launch_fwd_t<64, true>(tq, tk, tv, to, p, grid, stream)
+                      : launch_fwd_t<64, false>(tq, tk, tv, to, p, grid, stream);
+    return causal ? launch_fwd_t<128, true>(tq, tk, tv, to, p, grid, stream)
+                  : launch_fwd_t<128, false>(tq, tk, tv, to, p, grid, stream);
+}
+
+int fwd_take_status() {
+    int h = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&h, g_status_fwd, sizeof(int)) != cudaSuccess) return -5;
+    if (cudaMemcpyToSymbol(g_status_fwd, &z, sizeof(int)) != cudaSuccess) return -5;
+    return h;
+}
+
+}  // namespace fa

@@ -1,0 +1,28 @@
+// fa_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace fa {
+
+struct DebugKnobs {
+    unsigned long long timeout_ns;  // bound of every in-kernel wait
+    int inject;                     // fault-injection mode (0 = off)
+};
+
+// Status word values written by kernels (mirror of fa_status).
+constexpr int kStatusTimeout = -7;
+
+// Launchers: arguments already validated by the C-ABI layer.
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int D,
+               float scale, bool causal, cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+               void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
+               cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
+
+// Read and clear the device status word of each translation unit on the
+// current device (caller synchronises first).  Return 0 or a negative code.
+int fwd_take_status();
+int bwd_take_status();
+
+}  // namespace fa

@@ -1,0 +1,142 @@
+"""Forward parity: the CUDA forward (through the C ABI) against the fp64 CPU
+oracle on the same bf16 inputs.  Tolerances: O max-abs <= 1e-2, LSE max-abs
+<= 1e-3.  Small shapes are checked element by element over every output;
+the full-size workloads in the launch configuration the bench times are
+checked on sampled rows the oracle computes one by one."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import online_softmax_05_gb300 as fa
+from online_softmax_05_gb300.inputs import WORKLOADS, big_rows, make_inputs, to_f64, workload_inputs
+
+from tests.tolerances import LSE_TOL, O_TOL, o_ok
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from online_softmax_05_gb300 import build
+    build.build()
+    fa.load_library()
+
+
+def run_fwd(q, k, v, causal, scale):
+    dev = torch.device("cuda")
+    o, lse = fa.attention_forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    return to_f64(o.cpu()), lse.cpu().double().numpy()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257, 383, 500])
+def test_forward_small_shapes_full_compare(T, causal, D):
+    B, H = 1, 2
+    q, k, v, _ = make_inputs(B, H, T, D, seed=T + D)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_fwd(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attn_fwd(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+    assert o_ok(o, o_ref)
+    assert np.abs(lse - lse_ref).max() <= LSE_TOL
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("scale", [0.0, -0.07, 0.3])
+def test_forward_unusual_scales(scale):
+    B, H, T, D = 1, 1, 300, 64
+    q, k, v, _ = make_inputs(B, H, T, D, seed=5)
+    for causal in (False, True):
+        o, lse = run_fwd(q, k, v, causal, scale)
+        o_ref, lse_ref = oracle.attn_fwd(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+        assert o_ok(o, o_ref)
+        assert np.abs(lse - lse_ref).max() <= LSE_TOL
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 128, 129, 200, 3000])
+def test_mask_probe_uniform_scores(T, causal, D):
+    # Q = 0 makes every visible score 0, so P is uniform over the visible keys.
+    # With V[j] = e_{j mod D}: O[i, c] = #{visible j : j = c mod D} / #visible and
+    # LSE_i = log(#visible).  Which O entries are nonzero is an integer fact and
+    # must match exactly; the values match the closed form within tolerance.
+    B, H = 1, 1
+    q = torch.zeros(B, H, T, D, dtype=torch.bfloat16)
+    k = torch.randn(B, H, T, D, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    v = torch.zeros(B, H, T, D, dtype=torch.bfloat16)
+    v[0, 0, torch.arange(T), torch.arange(T) % D] = 1.0
+    o, lse = run_fwd(q, k, v, causal, 0.125)
+    i = np.arange(T)
+    n_vis = (i + 1) if causal else np.full(T, T)
+    counts = np.zeros((T, D))
+    for c in range(D):
+        # keys j < n_vis with j % D == c
+        counts[:, c] = np.maximum(0, (n_vis - 1 - c) // D + 1)
+    want = counts / n_vis[:, None]
+    np.testing.assert_array_equal(o[0, 0] != 0, want != 0)
+    assert np.abs(o[0, 0] - want).max() <= O_TOL
+    assert np.abs(lse[0, 0] - np.log(n_vis)).max() <= 1e-5
+
+
+@pytest.mark.gpu
+def test_forward_large_logits_growing_max():
+    # keys whose scores grow by hundreds from tile to tile: the deferred rescale must stay exact
+    B, H, T, D = 1, 2, 640, 128
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn(B, H, T, D, generator=g)
+    k = torch.randn(B, H, T, D, generator=g) * torch.linspace(0.1, 30.0, T)[None, None, :, None]
+    v = torch.randn(B, H, T, D, generator=g)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    for causal in (False, True):
+        o, lse = run_fwd(q, k, v, causal, 1.0 / math.sqrt(D))
+        o_ref, lse_ref = oracle.attn_fwd(to_f64(q), to_f64(k), to_f64(v), 1.0 / math.sqrt(D), causal)
+        assert o_ok(o, o_ref)
+        assert np.abs(lse - lse_ref).max() <= LSE_TOL
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["tiny_b1h2t128d64", "fwd_b1h8t1024d64"])
+def test_forward_workload_full_compare(name):
+    w = WORKLOADS[name]
+    q, k, v, _ = workload_inputs(w)
+    for causal in w.causal:
+        o, lse = run_fwd(q, k, v, causal, w.scale)
+        o_ref, lse_ref = oracle.attn_fwd(to_f64(q), to_f64(k), to_f64(v), w.scale, causal)
+        assert o_ok(o, o_ref)
+        assert np.abs(lse - lse_ref).max() <= LSE_TOL
+
+
+def sample_rows(T, n_random, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(range(min(T, 130))) | set(range(max(0, T - 130), T)) | set(rng.integers(0, T, n_random).tolist())
+    return np.array(sorted(rows))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["causal_b4h16t2048d64", "causal_b2h16t8192d128", "ragged_b8h32t3000d128"])
+def test_forward_workload_sampled_rows(name):
+    w = WORKLOADS[name]
+    q, k, v, _ = workload_inputs(w)
+    causal = w.causal[0]
+    o, lse = run_fwd(q, k, v, causal, w.scale)
+    BH = w.B * w.H
+    heads = {0, BH - 1, BH // 2 + 1}
+    extra_rows = {}
+    for flat in big_rows(w)[:6].tolist():   # heads holding x10 rows, and those rows
+        bh, t = divmod(flat, w.T)
+        heads.add(bh)
+        extra_rows.setdefault(bh, set()).add(t)
+    for bh in sorted(heads):
+        b, h = divmod(bh, w.H)
+        rows = np.array(sorted(set(sample_rows(w.T, 64, bh).tolist()) | extra_rows.get(bh, set())))
+        o_ref, lse_ref = oracle.attn_fwd_rows(to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h]), w.scale, causal,
+                                              rows)
+        assert o_ok(o[b, h, rows], o_ref), bh
+        assert np.abs(lse[b, h, rows] - lse_ref).max() <= LSE_TOL, bh
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
