@@ -1,0 +1,383 @@
+#!/usr/bin/env python3
+"""Throughput of the exact-attention hot path on GB300.
+
+One step = fa_fwd + fa_bwd (the whole path: forward with LSE, backward
+preprocess, fused key-outer backward, dQ conversion) over one batch of the
+long-context causal workload B=2, H=16, T=8192, D=128 (bf16, seeded
+synthetic inputs resident in HBM).  FLOPs are counted as the pages count
+them: forward 4*B*H*T^2*D, halved under causal masking; backward 2.5x the
+forward.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+N > 1 runs under torch.distributed.run: every rank processes its own
+independent batch (replicas, no collective on the data path); the barrier and
+max-over-ranks timing use NCCL.  Rank 0 prints ONE JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload, with the same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd & fwd+bwd (bf16, 1×GB300) and % of dense BF16 peak"
+DEFAULT_WORKLOAD = "causal_b2h16t8192d128"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+CLOCK_FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["online_softmax_05_gb300/csrc/fa_fwd.cu"],
+    "fa_bwd_main_kernel": ["online_softmax_05_gb300/csrc/fa_bwd.cu"],
+}
+COMMON_SOURCES = ["online_softmax_05_gb300/csrc/fa_ptx.cuh", "online_softmax_05_gb300/csrc/fa_sched.h",
+                  "online_softmax_05_gb300/csrc/fa_tmap.h"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload_flops(w, causal):
+    fwd = 4.0 * w.B * w.H * w.T * w.T * w.D / (2.0 if causal else 1.0)
+    return fwd, 2.5 * fwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(kernel):
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel] + COMMON_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[kernel]
+    except Exception:
+        return None
+    if d.get("source_sha256") != source_hash(kernel) or d.get("workload") != workload:
+        return None
+    return float(d["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    if self.uuid and self.uuid not in parts[0]:
+                        continue
+                    rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        reasons = sorted({name for r in rows for name, v in zip(REASON_NAMES, r[5:9]) if v.lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+_INPUT_CACHE = {}
+
+
+def time_oracle_heads(w, heads, causal, T=None):
+    """Run the fp64 oracle forward + backward on the given (b, h) heads
+    (optionally the first T tokens of each); returns (seconds, flops, threads)."""
+    import oracle
+    from online_softmax_05_gb300.inputs import to_f64, workload_inputs
+    oracle.build()
+    if _INPUT_CACHE.get("name") != w.name:
+        _INPUT_CACHE.clear()
+        _INPUT_CACHE.update(name=w.name, tensors=workload_inputs(w))
+    q, k, v, do = _INPUT_CACHE["tensors"]
+    T = T or w.T
+    arrays = [tuple(to_f64(t[b, h, :T]) for t in (q, k, v, do)) for b, h in heads]
+    t0 = time.perf_counter()
+    for qf, kf, vf, df in arrays:
+        oracle.attn_fwd(qf[None], kf[None], vf[None], w.scale, causal)
+        oracle.attn_bwd(qf[None], kf[None], vf[None], df[None], w.scale, causal)
+    sec = time.perf_counter() - t0
+    fwd = 4.0 * T * T * w.D / (2.0 if causal else 1.0)
+    return sec, 3.5 * fwd * len(heads), oracle.num_threads()
+
+
+def run_reference(args, w, causal, rank, world):
+    """Reference arm: the CPU oracle as it stands, bounded sample per step."""
+    if rank != 0:
+        return
+    # one head per step at full T costs ~5-10 s on 16 cores; shrink the causal
+    # prefix if the whole run would take more than about three minutes
+    n = args.steps + args.warmup
+    T_s = w.T
+    if n * 6.0 > 180.0:
+        T_s = max(256, int(w.T * math.sqrt(180.0 / (n * 6.0))) // 128 * 128)
+    BH = w.B * w.H
+    total_s, total_f, threads = 0.0, 0.0, 1
+    for s in range(n):
+        bh = s % BH
+        sec, fl, threads = time_oracle_heads(w, [divmod(bh, w.H)], causal, T_s)
+        if s >= args.warmup:
+            total_s += sec
+            total_f += fl
+    value = total_f / total_s / 1e12
+    sample = (f"per step one (b,h) head of {w.name} (round-robin over heads), "
+              + ("full T" if T_s == w.T else f"first {T_s} tokens (causal prefix)")
+              + ", fp64 oracle forward + backward (naive, materialises S and P)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "causal": causal,
+                       "passes": "fwd+bwd"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from online_softmax_05_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    causal = w.causal[0]
+
+    if args.impl == "reference":
+        run_reference(args, w, causal, rank, world)
+        return
+
+    import torch
+    import online_softmax_05_gb300 as fa
+    from online_softmax_05_gb300.inputs import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lib = fa.load_library()
+    stream = torch.cuda.current_stream(dev)
+
+    # seeded inputs, one independent batch per rank, resident in HBM
+    q, k, v, do = (t.to(dev) for t in make_inputs(w.B, w.H, w.T, w.D, seed=w.seed + rank, qk_std=w.qk_std,
+                                                   big_row_frac=w.big_row_frac, big_row_mult=w.big_row_mult))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.T, device=dev, dtype=torch.float32)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    B, H, T, D, scale = w.B, w.H, w.T, w.D, w.scale
+
+    def step():
+        rc = fa.fa_fwd(q, k, v, o, lse, B, H, T, D, scale, int(causal), stream)
+        if rc != 0:
+            raise fa.FAError(rc, "fa_fwd")
+        rc = fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, T, D, scale, int(causal), stream)
+        if rc != 0:
+            raise fa.FAError(rc, "fa_bwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_status(stream) != 0:
+        raise RuntimeError("device status reported a stalled kernel during warm-up")
+
+    # per-step events around the forward kernel and the backward's main kernel
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e4 in evs:
+        for e in e4:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid) as clocks:
+        t_start.record(stream)
+        for s in range(K):
+            lib.fa_set_timing_events(*(e.cuda_event for e in evs[s]))
+            step()
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    lib.fa_set_timing_events(None, None, None, None)
+    if dist is not None:
+        dist.barrier()
+    status = fa.fa_get_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    ms = t_start.elapsed_time(t_end) / K
+    fwd_ms = statistics.mean(evs[s][0].elapsed_time(evs[s][1]) for s in range(K))
+    bwd_ms = statistics.mean(evs[s][2].elapsed_time(evs[s][3]) for s in range(K))
+    if dist is not None:
+        tt = torch.tensor([ms, fwd_ms, bwd_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, fwd_ms, bwd_ms = tt.tolist()
+
+    fwd_fl, bwd_fl = workload_flops(w, causal)
+    step_fl = fwd_fl + bwd_fl
+    value = world * step_fl / (ms * 1e-3) / 1e12
+    fwd_tflops_kernel = fwd_fl / (fwd_ms * 1e-3) / 1e12
+    bwd_tflops_kernel = bwd_fl / (bwd_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak_sus, peak_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
+
+    def roofline(kernel, achieved):
+        return {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": achieved / peak_sus, "peak_kind": f"bf16 dense, sustained, of {peak_src}",
+                "frac_of_burst": achieved / peak_burst, "traffic": recorded_traffic(kernel, w.name)}
+
+    dominant_bwd = bwd_ms >= fwd_ms
+    rl_bwd = roofline("fa_bwd_main_kernel", bwd_tflops_kernel)
+    rl_fwd = roofline("fa_fwd_kernel", fwd_tflops_kernel)
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.to("cpu").pin_memory() for t in (q, k, v, do))
+        ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(4))
+        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        n_e2e = max(3, min(K, 20))
+
+        def e2e_step():
+            for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+                dst.copy_(src, non_blocking=True)
+            fa.attention_forward(q, k, v, causal=causal, scale=scale, out=o, lse=lse, stream=stream)
+            fa.attention_backward(q, k, v, o, lse, do, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv,
+                                  stream=stream)
+            for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b) / n_e2e
+        if dist is not None:
+            tt = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = tt.item()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+        e2e = {"value": world * step_fl / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads = [(0, 0), (0, 1)]
+        sec, fl, threads = time_oracle_heads(w, heads, causal)
+        cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"heads (b,h)={heads} of {w.name} at full T, fp64 oracle forward + backward "
+                         f"(naive, materialises S and P), {sec:.1f} s; FLOPs counted as for the GPU"}
+
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "causal": causal,
+                   "passes": "fwd+bwd", "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: inputs + outputs + workspace per step ~0.7 GB > 129 MB L2"},
+        "fwd_tflops": fwd_tflops_kernel, "fwd_ms": fwd_ms, "bwd_main_ms": bwd_ms,
+        "pct_of_peak": {"fwd_bwd_of_burst": 100 * value / world / peak_burst,
+                        "fwd_bwd_of_sustained": 100 * value / world / peak_sus,
+                        "fwd_of_burst": 100 * fwd_tflops_kernel / peak_burst, "peaks": peak_src},
+        "roofline": rl_bwd if dominant_bwd else rl_fwd,
+        "roofline_other": rl_fwd if dominant_bwd else rl_bwd,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * K,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

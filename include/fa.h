@@ -129,6 +129,17 @@ int fa_sched_tile_rows(int D, int* bm_fwd, int* bn, int* bm_bwd);
 int fa_debug_set_wait_timeout_ns(unsigned long long ns);
 int fa_debug_inject(int mode);
 
+/*
+ * Measurement hook (default off; host state read by each call).  When the
+ * pointers are non-NULL, later calls record these CUDA events (cudaEvent_t
+ * passed as void*, created and owned by the caller) on the call's stream:
+ * fwd_begin / fwd_end immediately around the forward kernel, bwd_begin /
+ * bwd_end immediately around the backward's main kernel (not its
+ * preprocess or dQ conversion).  Pass NULLs to turn it off.  Used to time
+ * the dominant kernel inside a timed region without a profiler.
+ */
+int fa_set_timing_events(void* fwd_begin, void* fwd_end, void* bwd_begin, void* bwd_end);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,15 +1,587 @@
-// fa_bwd.cu -- backward pass (placeholder until the kernels land).
+// fa_bwd.cu -- exact attention backward on sm_103a ("Lab 06 - Attention
+// kernels", section 4: D = rowsum(dO o O); P = exp(S - LSE) recomputed per
+// tile; dV = P^T dO; dP = dO V^T; dS = P o (dP - D); dQ = dS K scale;
+// dK = dS^T Q scale; key tiles outer, query tiles inner, so dK and dV
+// accumulate in one place while dQ receives a contribution from every key
+// tile).
+//
+// Three kernels on the caller's stream:
+//   fa_bwd_pre   D_i = sum_d dO_id O_id (fp32), LSE in log2 units, both
+//                padded to a multiple of 128 rows; zero the fp32 dQ
+//                accumulator.
+//   fa_bwd_main  one CTA per (key tile of 128, batch*head).  Warp roles:
+//                  warps 0-7   compute: P^T = exp2(S^T c - LSE2) and
+//                              dS^T = P^T o (dP^T - D) for half of the query
+//                              columns each (TMEM lane = key row)
+//                  warps 8-11  dQ drain (fp32 reductions into the
+//                              accumulator) and the dK/dV epilogue
+//                  warp 12     TMA producer (K, V once; Q, dO, LSE2, D per
+//                              query tile into a 2-stage ring)
+//                  warp 13     tcgen05 issuer
+//                Per query tile: S^T = K Q^T and dP^T = V dO^T into TMEM;
+//                dV += P^T dO with P^T read from TMEM; dK += dS^T Q and the
+//                dQ tile (dS K, or its transpose at D = 128) from dS^T in
+//                shared memory.
+//   fa_bwd_dq    dQ = bf16(dQacc * scale).
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_sched.h"
+#include "fa_tmap.h"
 
 namespace fa {
 
 static __device__ int g_status_bwd;
 
-int launch_bwd(const void*, const void*, const void*, const void*, const void*, const float*, void*, void*, void*,
-               int, int, int, int, float, bool, cudaStream_t, const DebugKnobs&, int) {
-    return -3;
+namespace {
+
+constexpr int kBwdThreads = 448;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int BM = bwd_bm(D);             // query rows per inner iteration
+    static constexpr int kHalf = BM / 2;             // query columns per compute warpgroup
+    static constexpr int kAtomsD = D / 64;
+    static constexpr bool kDqT = (D == 128);         // dQ^T = K^T dS^T (M = D) instead of dQ = dS K (M = BM)
+    static constexpr int kKVBytes = 128 * D * 2;     // one K or V tile
+    static constexpr int kQBytes = BM * D * 2;       // one Q or dO tile
+    static constexpr int kStages = 2;
+    static constexpr int kStageBytes = ((2 * kQBytes + 2 * BM * 4) + 1023) / 1024 * 1024;
+    static constexpr int kDSBytes = 128 * BM * 2;    // dS^T tile [128 keys][BM queries] bf16
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKVBytes;
+    static constexpr int kStageOff = 2 * kKVBytes;
+    static constexpr int kDSOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kBarOff = kDSOff + 2 * kDSBytes;
+    // kv_full, qdo_full[S], qdo_empty[S], s_full, dp_full, p_full, ds_empty[2], dq_full, dq_empty, dkv_full, mma_done
+    static constexpr int kNumBars = 1 + 2 * kStages + 3 + 2 + 4;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    // TMEM columns
+    static constexpr uint32_t kS = 0;                 // S^T  [128 keys][BM]   fp32
+    static constexpr uint32_t kDP = BM;               // dP^T [128 keys][BM]   fp32
+    static constexpr uint32_t kP = 2 * BM;            // P^T  [128 keys][BM]   bf16 pairs (BM/2 cols)
+    static constexpr uint32_t kDQ = 2 * BM + BM / 2;  // dQ^T [D][BM] or dQ [BM][D]: 64 columns
+    static constexpr uint32_t kDV = kDQ + 64;         // dV   [128 keys][D]    fp32
+    static constexpr uint32_t kDK = kDV + D;          // dK   [128 keys][D]    fp32
+    static_assert(kDK + D <= 512, "TMEM budget");
+    static constexpr uint32_t kIdescS = idesc_bf16_f32(128, BM, false, false);
+    static constexpr uint32_t kIdescDKV = idesc_bf16_f32(128, D, false, true);
+    static constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, 64, true, true);
+};
+
+struct BwdParams {
+    const float* lse2;   // [BH][T_pad] log2-domain LSE
+    const float* dvec;   // [BH][T_pad] D
+    float* dqacc;        // [BH][T][D]
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    int T, T_pad, BH, n_kt;
+    float scale;
+    float sl2, sl2_eff;
+    int prescale;
+    unsigned long long timeout_ns;
+};
+
+struct Ctl {
+    volatile int* abort;
+    unsigned long long timeout_ns;
+};
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
+    uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*c.abort) return false;
+        if (globaltimer_ns() - t0 > c.timeout_ns) {
+            *c.abort = 1;
+            atomicCAS(&g_status_bwd, 0, kStatusTimeout);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl c) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, c);
+}
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, c);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// ---------------------------------------------------------------- preprocess
+// D_i = rowsum(dO o O) ("Lab 06", section 4), LSE2 = LSE * log2(e); rows
+// t >= T of the padded vectors are 0; dQacc = 0.  8 elements per thread.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                         const __nv_bfloat16* __restrict__ dO,
+                                                         const float* __restrict__ lse, float* __restrict__ dvec,
+                                                         float* __restrict__ lse2, float* __restrict__ dqacc, int BH,
+                                                         int T, int T_pad) {
+    constexpr int TPR = D / 8;            // threads per row
+    constexpr int RPW = 32 / TPR;         // rows per warp
+    const long long total = static_cast<long long>(BH) * T_pad;
+    const int lane = threadIdx.x & 31, sub = lane % TPR;
+    const long long n_warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+    // warp-uniform loop: every lane reaches the shuffles below
+    for (long long wr = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; wr * RPW < total;
+         wr += n_warps) {
+        const long long r = wr * RPW + lane / TPR;
+        const bool in = r < total;
+        const int bh = in ? static_cast<int>(r / T_pad) : 0, t = in ? static_cast<int>(r % T_pad) : T_pad;
+        float acc = 0.f;
+        if (in && t < T) {
+            const size_t off = (static_cast<size_t>(bh) * T + t) * D + sub * 8;
+            const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+            const uint4 b = *reinterpret_cast<const uint4*>(dO + off);
+            const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+            const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 fa2 = __bfloat1622float2(pa[e]);
+                const float2 fb2 = __bfloat1622float2(pb[e]);
+                acc = fmaf(fa2.x, fb2.x, acc);
+                acc = fmaf(fa2.y, fb2.y, acc);
+            }
+            float4* z = reinterpret_cast<float4*>(dqacc + off);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, TPR);
+        if (in && sub == 0) {
+            dvec[r] = acc;
+            lse2[r] = (t < T) ? lse[static_cast<size_t>(bh) * T + t] * kLog2e : 0.f;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- dQ convert
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ dqacc,
+                                                        __nv_bfloat16* __restrict__ dq, long long n8, float scale) {
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4*>(dqacc)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(dqacc)[2 * i + 1];
+        uint4 w;
+        w.x = pack_bf16x2(a.x * scale, a.y * scale);
+        w.y = pack_bf16x2(a.z * scale, a.w * scale);
+        w.z = pack_bf16x2(b.x * scale, b.y * scale);
+        w.w = pack_bf16x2(b.z * scale, b.w * scale);
+        reinterpret_cast<uint4*>(dq)[i] = w;
+    }
+}
+
+// ---------------------------------------------------------------- main kernel
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       BwdParams p) {
+    using C = BwdCfg<D>;
+    constexpr int BM = C::BM;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sK = sbase + C::kKOff, sV = sbase + C::kVOff;
+    auto sQ = [&](int st) { return sbase + C::kStageOff + st * C::kStageBytes; };
+    auto sdO = [&](int st) { return sQ(st) + C::kQBytes; };
+    auto sLse = [&](int st) { return sQ(st) + 2 * C::kQBytes; };
+    auto sDv = [&](int st) { return sLse(st) + BM * 4; };
+    auto sDS = [&](int b) { return sbase + C::kDSOff + b * C::kDSBytes; };
+    const uint32_t bars = sbase + C::kBarOff;
+    const uint32_t kv_full = bars;
+    auto qdo_full = [&](int st) { return bars + 8u * (1 + st); };
+    auto qdo_empty = [&](int st) { return bars + 8u * (1 + C::kStages + st); };
+    const uint32_t s_full = bars + 8u * (1 + 2 * C::kStages);
+    const uint32_t dp_full = s_full + 8;
+    const uint32_t p_full = s_full + 16;
+    auto ds_empty = [&](int b) { return s_full + 24 + 8u * b; };
+    const uint32_t dq_full = s_full + 40;
+    const uint32_t dq_empty = s_full + 48;
+    const uint32_t dkv_full = s_full + 56;
+    const uint32_t mma_done = s_full + 64;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+    const Ctl ctl{abort_flag, p.timeout_ns};
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = p.T;
+    const int kt = blockIdx.x / p.BH, bh = blockIdx.x % p.BH;  // heavy key tiles (small kt) first
+    const int q_begin = bwd_q_begin(T, CAUSAL, kt, BM), q_end = bwd_q_end(T, BM);
+    const int n_it = q_end - q_begin;
+
+    if (tid == 0) {
+        mbar_init(kv_full, 1);
+        for (int st = 0; st < C::kStages; ++st) {
+            mbar_init(qdo_full(st), 1);
+            mbar_init(qdo_empty(st), 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_full, 8);
+        mbar_init(ds_empty(0), 1);
+        mbar_init(ds_empty(1), 1);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_empty, 4);
+        mbar_init(dkv_full, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 13) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp == 12) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t armed = 0;  // number of Q/dO fills issued
+            const uint64_t pol_kv = l2_policy_evict_first();
+            const uint64_t pol_q = l2_policy_evict_last();
+            mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
+            for (int a = 0; a < C::kAtomsD; ++a) {
+                tma_load_3d_hint(sK + a * 128 * 128, &tm_k, kv_full, 64 * a, kt * kBN, bh, pol_kv);
+                tma_load_3d_hint(sV + a * 128 * 128, &tm_v, kv_full, 64 * a, kt * kBN, bh, pol_kv);
+            }
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % C::kStages;
+                if (!wait_bar(qdo_empty(st), ((it / C::kStages) & 1) ^ 1, ctl)) break;
+                const int qt = q_begin + it;
+                const uint32_t fb = qdo_full(st);
+                mbar_arrive_expect_tx(fb, 2 * C::kQBytes + 2 * BM * 4);
+                ++armed;
+                for (int a = 0; a < C::kAtomsD; ++a) {
+                    tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qt * BM, bh, pol_q);
+                    tma_load_3d_hint(sdO(st) + a * BM * 128, &tm_do, fb, 64 * a, qt * BM, bh, pol_q);
+                }
+                const size_t voff = static_cast<size_t>(bh) * p.T_pad + static_cast<size_t>(qt) * BM;
+                bulk_load_1d(sLse(st), p.lse2 + voff, BM * 4, fb);
+                bulk_load_1d(sDv(st), p.dvec + voff, BM * 4, fb);
+            }
+            // drain: copies still in flight must land before the CTA exits
+            volatile int never = 0;
+            Ctl drain{&never, 100000000ull};
+            wait_bar(kv_full, 0, drain);
+            for (uint32_t f = armed > C::kStages ? armed - C::kStages : 0; f < armed; ++f)
+                wait_bar(qdo_full(f % C::kStages), (f / C::kStages) & 1, drain);
+        }
+    } else if (warp == 13) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            auto issue_sdp = [&](int st) {
+                // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = BM, K = D (both K-major)
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint32_t offk = (s >> 2) * (128 * 128) + (s & 3) * 32;
+                    const uint32_t offq = (s >> 2) * (BM * 128) + (s & 3) * 32;
+                    mma_ss(tmem + C::kS, sdesc_sw128(sK + offk, 16, 1024), sdesc_sw128(sQ(st) + offq, 16, 1024),
+                           C::kIdescS, s > 0);
+                }
+                mma_commit(s_full);
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint32_t offk = (s >> 2) * (128 * 128) + (s & 3) * 32;
+                    const uint32_t offq = (s >> 2) * (BM * 128) + (s & 3) * 32;
+                    mma_ss(tmem + C::kDP, sdesc_sw128(sV + offk, 16, 1024), sdesc_sw128(sdO(st) + offq, 16, 1024),
+                           C::kIdescS, s > 0);
+                }
+                mma_commit(dp_full);
+            };
+            if (!wait_bar(kv_full, 0, ctl)) goto mma_teardown;
+            if (!wait_bar(qdo_full(0), 0, ctl)) goto mma_teardown;
+            tc_fence_after();
+            issue_sdp(0);
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % C::kStages, b = it & 1;
+                if (!wait_bar(p_full, it & 1, ctl)) goto mma_teardown;
+                tc_fence_after();
+                // dV += P^T dO: A = P^T from TMEM, B = dO (MN-major: rows = queries = K)
+#pragma unroll
+                for (int s = 0; s < BM / 16; ++s)
+                    mma_ts(tmem + C::kDV, tmem + C::kP + s * 8, sdesc_sw128(sdO(st) + s * 2048, BM * 128, 1024),
+                           C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
+                if (it + 1 < n_it) {
+                    const int st1 = (it + 1) % C::kStages;
+                    if (!wait_bar(qdo_full(st1), ((it + 1) / C::kStages) & 1, ctl)) goto mma_teardown;
+                    tc_fence_after();
+                    issue_sdp(st1);
+                }
+                // dK += dS^T Q: A = dS^T (K-major over queries), B = Q (MN-major)
+#pragma unroll
+                for (int s = 0; s < BM / 16; ++s)
+                    mma_ss(tmem + C::kDK, sdesc_sw128(sDS(b) + (s >> 2) * (128 * 128) + (s & 3) * 32, 16, 1024),
+                           sdesc_sw128(sQ(st) + s * 2048, BM * 128, 1024), C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
+                if (it > 0) {
+                    if (!wait_bar(dq_empty, (it - 1) & 1, ctl)) goto mma_teardown;
+                    tc_fence_after();
+                }
+                // dQ tile over the 128 keys: both operands MN-major, K = keys
+#pragma unroll
+                for (int s = 0; s < 128 / 16; ++s) {
+                    if constexpr (C::kDqT)  // dQ^T [D][BM] = K^T dS^T
+                        mma_ss(tmem + C::kDQ, sdesc_sw128(sK + s * 2048, 128 * 128, 1024),
+                               sdesc_sw128(sDS(b) + s * 2048, 128 * 128, 1024), C::kIdescDQ, s > 0);
+                    else  // dQ [BM][D] = dS K
+                        mma_ss(tmem + C::kDQ, sdesc_sw128(sDS(b) + s * 2048, 128 * 128, 1024),
+                               sdesc_sw128(sK + s * 2048, 128 * 128, 1024), C::kIdescDQ, s > 0);
+                }
+                mma_commit(dq_full);
+                mma_commit(qdo_empty(st));
+                mma_commit(ds_empty(b));
+            }
+            mma_commit(dkv_full);
+        mma_teardown:
+            mma_commit(mma_done);
+            volatile int never = 0;
+            Ctl drain{&never, 100000000ull};
+            wait_bar(mma_done, 0, drain);
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ compute
+        const int h = warp >> 2, wq = warp & 3;
+        const int key = kt * kBN + 32 * wq + lane;
+        const uint32_t lane_base = tmem + ((32u * wq) << 16);
+        const float eff = p.sl2_eff;
+        for (int it = 0; it < n_it; ++it) {
+            const int st = it % C::kStages, b = it & 1;
+            const int qt = q_begin + it, q0 = qt * BM;
+            const bool masked = bwd_tile_class(T, CAUSAL, BM, qt, kt) == kMasked;
+            if (!warp_wait(qdo_full(st), (it / C::kStages) & 1, ctl)) break;
+            if (!warp_wait(s_full, it & 1, ctl)) break;
+            tc_fence_after();
+            const float* lse2 = reinterpret_cast<const float*>(smem + (sLse(st) - sbase));
+            const float* dvv = reinterpret_cast<const float*>(smem + (sDv(st) - sbase));
+            float pf[C::kHalf];
+#pragma unroll
+            for (int ch = 0; ch < C::kHalf / 32; ++ch) {
+                const int c0 = h * C::kHalf + 32 * ch;  // first query column of this chunk
+                uint32_t sr[32];
+                tmem_ld32(lane_base + C::kS + c0, sr);
+                tmem_ld_wait();
+                reg_fence32(sr);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float s = __uint_as_float(sr[e]);
+                    if (p.prescale) s *= p.sl2;
+                    float pv = ex2_approx(fmaf(s, eff, -lse2[c0 + e]));
+                    if (masked && !bwd_elem_visible(T, CAUSAL, q0 + c0 + e, key)) pv = 0.f;
+                    pf[32 * ch + e] = pv;
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]);
+                tmem_st16(lane_base + C::kP + c0 / 2, pk);
+            }
+            if (!warp_wait(dp_full, it & 1, ctl)) break;
+            if (!warp_wait(ds_empty(b), ((it >> 1) & 1) ^ 1, ctl)) break;
+            tc_fence_after();
+            const uint32_t ds_base = sDS(b);
+#pragma unroll
+            for (int ch = 0; ch < C::kHalf / 32; ++ch) {
+                const int c0 = h * C::kHalf + 32 * ch;
+                uint32_t dr[32];
+                tmem_ld32(lane_base + C::kDP + c0, dr);
+                tmem_ld_wait();
+                reg_fence32(dr);
+                // dS^T row `key`, query columns c0 .. c0+31 -> 4 chunks of 8 in the swizzled tile
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 8 * g + 2 * e;
+                        const float d0 = pf[32 * ch + c] * (__uint_as_float(dr[c]) - dvv[c0 + c]);
+                        const float d1 = pf[32 * ch + c + 1] * (__uint_as_float(dr[c + 1]) - dvv[c0 + c + 1]);
+                        w4[e] = pack_bf16x2(d0, d1);
+                    }
+                    const int col = c0 + 8 * g;
+                    st_shared_v4(ds_base + (col >> 6) * (128 * 128) + sw128_off(32 * wq + lane, (col & 63) >> 3),
+                                 w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+    } else {
+        // ------------------------------------------------------------ dQ drain + dK/dV epilogue (warps 8-11)
+        const int wq = warp - 8;
+        const uint32_t lane_base = tmem + ((32u * wq) << 16);
+        const int r = 32 * wq + lane;  // TMEM lane of this thread
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int q0 = (q_begin + it) * BM;
+            if (!warp_wait(dq_full, it & 1, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + C::kDQ + 32 * ch, v);
+                tmem_ld_wait();
+                reg_fence32(v);
+                if constexpr (C::kDqT) {
+                    // lane = d; columns = queries q0 + 32 ch + e
+                    float* base = p.dqacc + (static_cast<size_t>(bh) * T + q0 + 32 * ch) * D + r;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (q0 + 32 * ch + e < T) atomicAdd(base + static_cast<size_t>(e) * D, __uint_as_float(v[e]));
+                } else {
+                    // lane = query row q0 + r; columns = d
+                    if (q0 + r < T) {
+                        float* base = p.dqacc + (static_cast<size_t>(bh) * T + q0 + r) * D + 32 * ch;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            red_add_v4_f32(base + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                           __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dq_empty);
+        }
+        if (ok && warp_wait(dkv_full, 0, ctl)) {
+            tc_fence_after();
+            const int key = kt * kBN + r;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which ? C::kDV : C::kDK;
+                const float mul = which ? 1.f : p.scale;
+                __nv_bfloat16* out = which ? p.dv : p.dk;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_base + col + 32 * ch, v);
+                    tmem_ld_wait();
+                    reg_fence32(v);
+                    if (key < T) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * T + key) * D + 32 * ch);
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]) * mul, __uint_as_float(v[8 * g + 1]) * mul);
+                            w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]) * mul, __uint_as_float(v[8 * g + 3]) * mul);
+                            w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]) * mul, __uint_as_float(v[8 * g + 5]) * mul);
+                            w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]) * mul, __uint_as_float(v[8 * g + 7]) * mul);
+                            dst[g] = w;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 13) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool CAUSAL>
+int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                  const BwdParams& p, cudaStream_t st) {
+    static bool attr_set = false;
+    auto kern = fa_bwd_main_kernel<D, CAUSAL>;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes) !=
+            cudaSuccess)
+            return -5;
+        attr_set = true;
+    }
+    kern<<<p.n_kt * p.BH, kBwdThreads, BwdCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+}  // namespace
+
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+               void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
+               cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
+    const int BH = B * H;
+    const int T_pad = cdiv(T, 128) * 128;
+    const size_t n_vec = static_cast<size_t>(BH) * T_pad;
+    const size_t n_acc = static_cast<size_t>(BH) * T * D;
+    const size_t bytes_vec = (n_vec * 4 + 255) / 256 * 256;
+    const size_t bytes = 2 * bytes_vec + n_acc * 4;
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return -6;
+    }
+    float* dvec = static_cast<float*>(ws);
+    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_vec);
+    float* dqacc = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * bytes_vec);
+    int rc = 0;
+    CUtensorMap tq, tk, tv, tdo;
+    const int bm = bwd_bm(D);
+    if (!make_tmap_bhtd(&tq, q, BH, T, D, bm) || !make_tmap_bhtd(&tk, k, BH, T, D, 128) ||
+        !make_tmap_bhtd(&tv, v, BH, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, bm)) {
+        rc = -5;
+    } else {
+        const long long rows = static_cast<long long>(BH) * T_pad;
+        const int tpr = D / 8;
+        long long blocks = (rows * tpr + 255) / 256;
+        const int pre_grid = static_cast<int>(blocks < 8LL * num_sms ? blocks : 8LL * num_sms);
+        if (D == 64)
+            fa_bwd_pre_kernel<64><<<pre_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                                static_cast<const __nv_bfloat16*>(dO), lse, dvec,
+                                                                lse2, dqacc, BH, T, T_pad);
+        else
+            fa_bwd_pre_kernel<128><<<pre_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                                 static_cast<const __nv_bfloat16*>(dO), lse, dvec,
+                                                                 lse2, dqacc, BH, T, T_pad);
+        if (cudaGetLastError() != cudaSuccess) rc = -5;
+        if (rc == 0) {
+            BwdParams p;
+            p.lse2 = lse2;
+            p.dvec = dvec;
+            p.dqacc = dqacc;
+            p.dk = static_cast<__nv_bfloat16*>(dk);
+            p.dv = static_cast<__nv_bfloat16*>(dv);
+            p.T = T;
+            p.T_pad = T_pad;
+            p.BH = BH;
+            p.n_kt = cdiv(T, kBN);
+            p.scale = scale;
+            p.sl2 = scale * kLog2e;
+            p.prescale = p.sl2 > 0.f ? 0 : 1;
+            p.sl2_eff = p.prescale ? 1.f : p.sl2;
+            p.timeout_ns = dbg.timeout_ns;
+            if (dbg.ev[2]) cudaEventRecord(dbg.ev[2], stream);
+            if (D == 64)
+                rc = causal ? launch_main_t<64, true>(tq, tk, tv, tdo, p, stream)
+                            : launch_main_t<64, false>(tq, tk, tv, tdo, p, stream);
+            else
+                rc = causal ? launch_main_t<128, true>(tq, tk, tv, tdo, p, stream)
+                            : launch_main_t<128, false>(tq, tk, tv, tdo, p, stream);
+            if (dbg.ev[3]) cudaEventRecord(dbg.ev[3], stream);
+        }
+        if (rc == 0) {
+            const long long n8 = static_cast<long long>(n_acc / 8);
+            long long blocks8 = (n8 + 255) / 256;
+            const int g = static_cast<int>(blocks8 < 8LL * num_sms ? blocks8 : 8LL * num_sms);
+            fa_bwd_dq_kernel<<<g, 256, 0, stream>>>(dqacc, static_cast<__nv_bfloat16*>(dq), n8, scale);
+            if (cudaGetLastError() != cudaSuccess) rc = -5;
+        }
+    }
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == 0) rc = -5;
+    return rc;
 }
 
 int bwd_take_status() {

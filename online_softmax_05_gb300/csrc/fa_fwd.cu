@@ -11,18 +11,20 @@
 //   warp 8     TMA producer: Q tiles once per item, K/V tiles into a ring
 //   warp 9     tcgen05 issuer: S = Q K^T into TMEM, O += P V with P in TMEM
 // Per key tile j the softmax warps read S_t(j) from TMEM, update the running
-// max m (log2 domain, scale*log2(e) folded in), rescale O only when m grows
-// by more than 2^8 (exact, see below), write P = exp2(S*c - m) as bf16 back
+// max m (log2 domain, scale*log2(e) folded in), rescale O when m grows
+// (see the rescale policy below), write P = exp2(S*c - m) as bf16 back
 // into the same TMEM columns and hand it to the MMA warp.  The two query
 // tiles ping-pong: the softmax of one overlaps the tensor-core work of the
 // other.  Finally O = acc / l goes out through shared memory with a TMA store
 // and LSE = (m + log2 l) * ln 2 is written per row.
 //
-// Deferred rescale: O = acc / l and LSE = m_used + log l hold for ANY
-// reference m_used, since e^{x - m} = e^{m' - m} e^{x - m'} ("Lab 06",
-// section 2, "Why the rescale is exact").  Keeping m_used while the true max
-// exceeds it by at most 8 (log2 units) bounds every P by 2^8, far from
-// overflow in fp32 and bf16.
+// Rescale policy: O = acc / l and LSE = m_used + log l hold for ANY
+// reference m_used ("Lab 06", section 2, "Why the rescale is exact"), so the
+// rescale could be deferred while the max grows by less than a threshold.
+// It is not: P is rounded to bf16 before P V, and a dominant weight
+// 2^delta (0 < delta) is not a bf16 number, so a near-one-hot row would
+// carry up to 2^-9 relative error in O.  With the reference equal to the
+// running max the dominant weight is exp2(0) = 1, exact in bf16.
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
@@ -37,7 +39,7 @@ static __device__ int g_status_fwd;
 namespace {
 
 constexpr int kFwdThreads = 320;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleThreshold = 0.0f;  // log2 units; see the rescale policy above
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -487,11 +489,16 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     p.timeout_ns = dbg.timeout_ns;
     p.inject = dbg.inject;
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+    if (dbg.ev[0]) cudaEventRecord(dbg.ev[0], stream);
+    int rc;
     if (D == 64)
-        return causal ? launch_fwd_t<64, true>(tq, tk, tv, to, p, grid, stream)
-                      : launch_fwd_t<64, false>(tq, tk, tv, to, p, grid, stream);
-    return causal ? launch_fwd_t<128, true>(tq, tk, tv, to, p, grid, stream)
-                  : launch_fwd_t<128, false>(tq, tk, tv, to, p, grid, stream);
+        rc = causal ? launch_fwd_t<64, true>(tq, tk, tv, to, p, grid, stream)
+                    : launch_fwd_t<64, false>(tq, tk, tv, to, p, grid, stream);
+    else
+        rc = causal ? launch_fwd_t<128, true>(tq, tk, tv, to, p, grid, stream)
+                    : launch_fwd_t<128, false>(tq, tk, tv, to, p, grid, stream);
+    if (dbg.ev[1]) cudaEventRecord(dbg.ev[1], stream);
+    return rc;
 }
 
 int fwd_take_status() {

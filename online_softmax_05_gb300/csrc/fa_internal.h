@@ -8,6 +8,7 @@ namespace fa {
 struct DebugKnobs {
     unsigned long long timeout_ns;  // bound of every in-kernel wait
     int inject;                     // fault-injection mode (0 = off)
+    cudaEvent_t ev[4];              // measurement hook: fwd begin/end, bwd-main begin/end (may be null)
 };
 
 // Status word values written by kernels (mirror of fa_status).

@@ -12,6 +12,11 @@ import numpy as np
 O_TOL = 1e-2
 LSE_TOL = 1e-3
 GRAD_REL_TOL = 2e-2
+# When the exact gradient is identically zero (every row sees a single key,
+# e.g. T = 1: P = 1 and dS = P (dP - D) = 0), 2e-2 * max|grad| is 0.  D and
+# dP are the same fp32 sum taken in different orders, so a residual of fp32
+# rounding remains; this absolute floor only matters in that degenerate case.
+GRAD_ABS_FLOOR = 1e-5
 
 
 def bf16_half_ulp(x):
@@ -30,6 +35,10 @@ def o_ok(o, o_ref):
     return bool(np.all(np.abs(np.asarray(o) - o_ref) <= o_bound(o_ref)))
 
 
+def grad_bound(g_ref):
+    return max(GRAD_REL_TOL * float(np.abs(np.asarray(g_ref, dtype=np.float64)).max()), GRAD_ABS_FLOOR)
+
+
 def grad_ok(g, g_ref):
     g_ref = np.asarray(g_ref, dtype=np.float64)
-    return bool(np.abs(np.asarray(g) - g_ref).max() <= GRAD_REL_TOL * np.abs(g_ref).max())
+    return bool(np.abs(np.asarray(g) - g_ref).max() <= grad_bound(g_ref))
