@@ -54,7 +54,8 @@ typedef enum fa_status {
     FA_ERR_NOMEM = -6,           /* stream-ordered workspace allocation failed */
     FA_ERR_DEVICE_TIMEOUT = -7,  /* a kernel's bounded wait ran out (pipeline stall); outputs invalid */
     FA_ERR_ARG = -8,             /* causal not 0/1, or scale not finite */
-    FA_ERR_ARCH = -9             /* current device is not compute capability 10.3 (sm_103a) */
+    FA_ERR_ARCH = -9,            /* current device is not compute capability 10.3 (sm_103a) */
+    FA_ERR_SCRATCH = -10         /* fa_bwd_noalloc: problem needs more than its fixed scratch buffer */
 } fa_status;
 
 /*
@@ -82,6 +83,37 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, void* dq, void* dk, void* dv,
            int B, int H, int T, int D, float scale, int causal, void* stream);
+
+/*
+ * Backward pass that allocates nothing.  The pages have no counterpart to
+ * this entry point: it exists for callers that cannot allocate device memory
+ * at call time, for example code running inside a memory pool that must not
+ * grow, or a runtime whose allocator is not reachable from the calling
+ * thread.  fa_bwd takes its workspace with cudaMallocAsync; this variant
+ * instead uses a fixed scratch buffer compiled into the library
+ * (FA_BWD_NOALLOC_SCRATCH_BYTES = 64 MiB of device memory, reserved on every
+ * GPU that loads the library's backward module, held until the process
+ * exits).  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Same arguments, layout, results and asynchrony as fa_bwd.  The caller
+ * still owns every input and output.
+ * Limit: 8 * B*H*T_pad + 4 * B*H*T*D bytes must not exceed the scratch size,
+ *   where T_pad is T rounded up to a multiple of 128 (roughly
+ *   B*H*T*D <= 16 M elements at D = 128); larger problems return
+ *   FA_ERR_SCRATCH and nothing is enqueued.
+ * Set-up: the first call on each device looks up the buffer's device
+ *   address (cudaGetSymbolAddress); make that first call before any stream
+ *   capture.
+ * Sharing: every call uses the same buffer, which keeps the previous call's
+ *   contents (the backward clears what must start at zero).  Calls whose
+ *   work overlaps on the GPU (different streams, or different host threads
+ *   without ordering) race on the buffer and corrupt each other's results;
+ *   serialise them.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   int B, int H, int T, int D, float scale, int causal, void* stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* fa_strerror(int status);

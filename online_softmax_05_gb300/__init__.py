@@ -12,7 +12,7 @@ import math
 import os
 import threading
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_strerror", "fa_get_device_status", "fa_version",
+__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
            "attention_forward", "attention_backward", "FAError", "library_path", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -23,7 +23,7 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_SHAPE", -3: "FA_ERR_UNSUPPORTED", -4: "FA_ERR_ALIGN",
                 -5: "FA_ERR_CUDA", -6: "FA_ERR_NOMEM", -7: "FA_ERR_DEVICE_TIMEOUT", -8: "FA_ERR_ARG",
-                -9: "FA_ERR_ARCH"}
+                -9: "FA_ERR_ARCH", -10: "FA_ERR_SCRATCH"}
 
 
 class FAError(RuntimeError):
@@ -51,6 +51,8 @@ def load_library():
         lib.fa_fwd.restype = i
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         lib.fa_bwd.restype = i
+        lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.fa_bwd_noalloc.restype = i
         lib.fa_strerror.argtypes = [i]
         lib.fa_strerror.restype = ctypes.c_char_p
         lib.fa_get_device_status.argtypes = [vp]
@@ -102,6 +104,15 @@ def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B: int, H: int, T: int, D: int, scal
     """C-ABI ``fa_bwd``; tensors (or raw device pointers) in, status code out."""
     return load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
                                  _ptr(dv), B, H, T, D, float(scale), int(causal), _stream(stream))
+
+
+def fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B: int, H: int, T: int, D: int, scale: float, causal: int,
+                   stream=None) -> int:
+    """C-ABI ``fa_bwd_noalloc``: fa_bwd without any device allocation, for
+    callers that cannot allocate at call time; uses the library's fixed
+    64 MiB scratch buffer (one shared buffer: serialise calls)."""
+    return load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), B, H, T, D, float(scale), int(causal), _stream(stream))
 
 
 def fa_strerror(code: int) -> str:

@@ -89,6 +89,7 @@ const char* fa_strerror(int status) {
         case FA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out (pipeline stall); outputs are invalid";
         case FA_ERR_ARG: return "causal must be 0 or 1, scale finite, and outputs must not overlap other buffers";
         case FA_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
+        case FA_ERR_SCRATCH: return "fa_bwd_noalloc: the problem needs more than the fixed 64 MiB scratch buffer";
         default: return "unknown fa_status";
     }
 }
@@ -135,6 +136,34 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     if (rc != FA_OK) return rc;
     return fa::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, T, D, scale, causal != 0,
                           static_cast<cudaStream_t>(stream), knobs(), sms);
+}
+
+// Same checks as fa_bwd, then the fixed-scratch backward (see include/fa.h:
+// for callers that cannot allocate device memory at call time).
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+    int rc = check_shape(B, H, T, D, scale, causal);
+    if (rc != FA_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(B) * H * T * D * 2, nl = static_cast<size_t>(B) * H * T * 4;
+    const Range ins[6] = {range_of(q, n), range_of(k, n), range_of(v, n), range_of(o, n), range_of(dO, n),
+                          range_of(lse, nl)};
+    const Range outs[3] = {range_of(dq, n), range_of(dk, n), range_of(dv, n)};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlap(outs[a], ins[b])) return FA_ERR_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlap(outs[a], outs[b])) return FA_ERR_ARG;
+    }
+    if (fa::bwd_scratch_bytes(B, H, T, D) > FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH;
+    int dev = 0, sms = 0;
+    rc = current_device(&dev, &sms);
+    if (rc != FA_OK) return rc;
+    return fa::launch_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, T, D, scale, causal != 0,
+                                  static_cast<cudaStream_t>(stream), knobs(), sms);
 }
 
 int fa_get_device_status(void* stream) {

@@ -25,6 +25,9 @@
 //   fa_bwd_dq    dQ = bf16(dQacc * scale).
 #include <cuda_runtime.h>
 
+#include <mutex>
+
+#include "fa.h"
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 #include "fa_sched.h"
@@ -582,6 +585,102 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
     }
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == 0) rc = -5;
     return rc;
+}
+
+// ---------------------------------------------------------------- fixed scratch
+// Workspace for fa_bwd_noalloc, for callers that cannot allocate device
+// memory at call time.  It lives in the module's global memory, so every GPU
+// that loads this module holds it until the process exits.  Kernels receive
+// its device address from the host; the host-side symbol itself is only a
+// stand-in and must never be passed to a kernel.
+static __device__ __align__(256) unsigned char g_bwd_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kScratchMaxDevices = 64;
+std::once_flag g_scratch_once[kScratchMaxDevices];
+void* g_scratch_ptr[kScratchMaxDevices];
+cudaError_t g_scratch_err[kScratchMaxDevices];
+
+// Device address of g_bwd_scratch on the current device, looked up once per
+// device (the first fa_bwd_noalloc call on that device does it).
+void* scratch_address(int dev) {
+    std::call_once(g_scratch_once[dev], [dev] {
+        void* p = nullptr;
+        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_bwd_scratch);
+        g_scratch_ptr[dev] = p;
+    });
+    return g_scratch_err[dev] == cudaSuccess ? g_scratch_ptr[dev] : nullptr;
+}
+}  // namespace
+
+size_t bwd_scratch_bytes(int B, int H, int T, int D) {
+    const size_t BH = static_cast<size_t>(B) * H;
+    const size_t T_pad = static_cast<size_t>(cdiv(T, 128)) * 128;
+    const size_t bytes_vec = (BH * T_pad * 4 + 255) / 256 * 256;
+    return 2 * bytes_vec + BH * static_cast<size_t>(T) * D * 4;
+}
+
+int launch_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                       void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
+                       cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
+    if (bwd_scratch_bytes(B, H, T, D) > FA_BWD_NOALLOC_SCRATCH_BYTES) return -10;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchMaxDevices) return -5;
+    void* ws = scratch_address(dev);
+    if (!ws) return -5;
+    const int BH = B * H;
+    const int T_pad = cdiv(T, 128) * 128;
+    const size_t bytes_vec = (static_cast<size_t>(BH) * T_pad * 4 + 255) / 256 * 256;
+    const size_t n_acc = static_cast<size_t>(BH) * T * D;
+    float* dvec = static_cast<float*>(ws);
+    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_vec);
+    float* dqacc = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * bytes_vec);
+    CUtensorMap tq, tk, tv, tdo;
+    const int bm = bwd_bm(D);
+    if (!make_tmap_bhtd(&tq, q, BH, T, D, bm) || !make_tmap_bhtd(&tk, k, BH, T, D, 128) ||
+        !make_tmap_bhtd(&tv, v, BH, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, bm))
+        return -5;
+    // preprocess clears the accumulator, so the previous call's contents do not matter
+    const long long rows = static_cast<long long>(BH) * T_pad;
+    const long long blocks = (rows * (D / 8) + 255) / 256;
+    const int pre_grid = static_cast<int>(blocks < 8LL * num_sms ? blocks : 8LL * num_sms);
+    if (D == 64)
+        fa_bwd_pre_kernel<64><<<pre_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                            static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2,
+                                                            dqacc, BH, T, T_pad);
+    else
+        fa_bwd_pre_kernel<128><<<pre_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                             static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2,
+                                                             dqacc, BH, T, T_pad);
+    if (cudaGetLastError() != cudaSuccess) return -5;
+    BwdParams p;
+    p.lse2 = lse2;
+    p.dvec = dvec;
+    p.dqacc = dqacc;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.T = T;
+    p.T_pad = T_pad;
+    p.BH = BH;
+    p.n_kt = cdiv(T, kBN);
+    p.scale = scale;
+    p.sl2 = scale * kLog2e;
+    p.prescale = p.sl2 > 0.f ? 0 : 1;
+    p.sl2_eff = p.prescale ? 1.f : p.sl2;
+    p.timeout_ns = dbg.timeout_ns;
+    int rc;
+    if (D == 64)
+        rc = causal ? launch_main_t<64, true>(tq, tk, tv, tdo, p, stream)
+                    : launch_main_t<64, false>(tq, tk, tv, tdo, p, stream);
+    else
+        rc = causal ? launch_main_t<128, true>(tq, tk, tv, tdo, p, stream)
+                    : launch_main_t<128, false>(tq, tk, tv, tdo, p, stream);
+    if (rc != 0) return rc;
+    const long long n8 = static_cast<long long>(n_acc / 8);
+    const long long blocks8 = (n8 + 255) / 256;
+    const int g = static_cast<int>(blocks8 < 8LL * num_sms ? blocks8 : 8LL * num_sms);
+    fa_bwd_dq_kernel<<<g, 256, 0, stream>>>(dqacc, static_cast<__nv_bfloat16*>(dq), n8, scale);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
 int bwd_take_status() {

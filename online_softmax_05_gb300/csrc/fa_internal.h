@@ -21,6 +21,13 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
                void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
                cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
 
+// Backward with the library's fixed device scratch buffer instead of an
+// allocation; returns -10 if the problem does not fit, without launching.
+size_t bwd_scratch_bytes(int B, int H, int T, int D);
+int launch_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                       void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
+                       cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
+
 // Read and clear the device status word of each translation unit on the
 // current device (caller synchronises first).  Return 0 or a negative code.
 int fwd_take_status();
