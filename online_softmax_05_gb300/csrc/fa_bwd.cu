@@ -16,7 +16,7 @@
 //                  warps 8-11  dQ drain (fp32 reductions into the
 //                              accumulator) and the dK/dV epilogue
 //                  warp 12     TMA producer (K, V once; Q, dO, LSE2, D per
-//                              query tile into a 2-stage ring)
+//                              query tile into a 3-stage ring)
 //                  warp 13     tcgen05 issuer
 //                Per query tile: S^T = K Q^T and dP^T = V dO^T into TMEM;
 //                dV += P^T dO with P^T read from TMEM; dK += dS^T Q and the
@@ -37,7 +37,29 @@ namespace fa {
 
 static __device__ int g_status_bwd;
 
+// Optional cycle tracing of one CTA's pipeline (build with -DFA_TRACE; off in
+// the library): slot = event kind, index = query-tile iteration.
+#ifdef FA_TRACE
+constexpr int kTraceSlots = 28, kTraceLen = 512;
+static __device__ unsigned long long g_trace[kTraceSlots][kTraceLen];
+#define FA_TRACE_EVENT(slot, idx)                                                  \
+    do {                                                                           \
+        if (blockIdx.x == 0 && (idx) < kTraceLen) g_trace[slot][idx] = clock64(); \
+    } while (0)
+#else
+#define FA_TRACE_EVENT(slot, idx) \
+    do {                          \
+    } while (0)
+#endif
+
 namespace {
+
+#ifndef FA_CRIT_SLEEP
+#define FA_CRIT_SLEEP 0
+#endif
+// Waits on the MMA <-> compute critical path poll back to back unless built
+// with FA_CRIT_SLEEP=1; every other wait lets the hardware park the thread.
+constexpr bool kCritSleep = FA_CRIT_SLEEP != 0;
 
 constexpr int kBwdThreads = 448;
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -48,9 +70,13 @@ struct BwdCfg {
     static constexpr int kHalf = BM / 2;             // query columns per compute warpgroup
     static constexpr int kAtomsD = D / 64;
     static constexpr bool kDqT = (D == 128);         // dQ^T = K^T dS^T (M = D) instead of dQ = dS K (M = BM)
+    // D = 128: two S^T buffers, P^T aliased into the S buffer it came from at
+    // column offset BM/4 (each compute warpgroup then overwrites only columns
+    // it has itself already read).  D = 64: one S^T buffer, P^T in its own region.
+    static constexpr bool kSDouble = (D == 128);
     static constexpr int kKVBytes = 128 * D * 2;     // one K or V tile
     static constexpr int kQBytes = BM * D * 2;       // one Q or dO tile
-    static constexpr int kStages = 2;
+    static constexpr int kStages = 3;
     static constexpr int kStageBytes = ((2 * kQBytes + 2 * BM * 4) + 1023) / 1024 * 1024;
     static constexpr int kDSBytes = 128 * BM * 2;    // dS^T tile [128 keys][BM queries] bf16
     static constexpr int kKOff = 0;
@@ -58,17 +84,19 @@ struct BwdCfg {
     static constexpr int kStageOff = 2 * kKVBytes;
     static constexpr int kDSOff = kStageOff + kStages * kStageBytes;
     static constexpr int kBarOff = kDSOff + 2 * kDSBytes;
-    // kv_full, qdo_full[S], qdo_empty[S], s_full, dp_full, p_full, ds_empty[2], dq_full, dq_empty, dkv_full, mma_done
-    static constexpr int kNumBars = 1 + 2 * kStages + 3 + 2 + 4;
+    // kv_full, qdo_full[S], qdo_empty[S], s_full[2], dp_full, p_full, ds_empty[2], dq_full, dq_empty,
+    // dkv_full, mma_done, p_free
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 5;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
     // TMEM columns
-    static constexpr uint32_t kS = 0;                 // S^T  [128 keys][BM]   fp32
-    static constexpr uint32_t kDP = BM;               // dP^T [128 keys][BM]   fp32
-    static constexpr uint32_t kP = 2 * BM;            // P^T  [128 keys][BM]   bf16 pairs (BM/2 cols)
-    static constexpr uint32_t kDQ = 2 * BM + BM / 2;  // dQ^T [D][BM] or dQ [BM][D]: 64 columns
-    static constexpr uint32_t kDV = kDQ + 64;         // dV   [128 keys][D]    fp32
-    static constexpr uint32_t kDK = kDV + D;          // dK   [128 keys][D]    fp32
+    static constexpr uint32_t kS = 0;                                  // S^T [128 keys][BM] fp32 (x2 at D = 128)
+    static constexpr uint32_t kDP = kSDouble ? 2 * BM : BM;            // dP^T [128 keys][BM] fp32
+    static constexpr uint32_t kP = kDP + BM;                           // P^T bf16 pairs (single-S layout only)
+    static constexpr uint32_t kDQ = kSDouble ? kDP + BM : kP + BM / 2; // dQ^T [D][BM] or dQ [BM][D]: 64 columns
+    static constexpr uint32_t kDV = kDQ + 64;                          // dV [128 keys][D] fp32
+    static constexpr uint32_t kDK = kDV + D;                           // dK [128 keys][D] fp32
     static_assert(kDK + D <= 512, "TMEM budget");
     static constexpr uint32_t kIdescS = idesc_bf16_f32(128, BM, false, false);
     static constexpr uint32_t kIdescDKV = idesc_bf16_f32(128, D, false, true);
@@ -93,10 +121,15 @@ struct Ctl {
     unsigned long long timeout_ns;
 };
 
+// Slow path of a bounded wait.  kSleep: the hardware suspends the polling
+// thread between checks (for waits off the critical path, so that polling
+// does not take issue slots from busy warps on the same sub-partition);
+// otherwise the thread polls back to back (lowest wake-up latency).
+template <bool kSleep>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
     uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (kSleep ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
         if (*c.abort) return false;
         if (globaltimer_ns() - t0 > c.timeout_ns) {
             *c.abort = 1;
@@ -105,13 +138,17 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
         }
     }
 }
+// Bounded wait: true when the phase completed, false when the CTA aborted
+// (this wait ran out of time, or another role already gave up).
+template <bool kSleep = true>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl c) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, c);
+    return wait_slow<kSleep>(bar, parity, c);
 }
+template <bool kSleep = true>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, c);
+    if ((threadIdx.x & 31) == 0) ok = wait_bar<kSleep>(bar, parity, c);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -186,6 +223,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        BwdParams p) {
     using C = BwdCfg<D>;
     constexpr int BM = C::BM;
+    constexpr int NST = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -198,32 +236,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t bars = sbase + C::kBarOff;
     const uint32_t kv_full = bars;
     auto qdo_full = [&](int st) { return bars + 8u * (1 + st); };
-    auto qdo_empty = [&](int st) { return bars + 8u * (1 + C::kStages + st); };
-    const uint32_t s_full = bars + 8u * (1 + 2 * C::kStages);
-    const uint32_t dp_full = s_full + 8;
-    const uint32_t p_full = s_full + 16;
-    auto ds_empty = [&](int b) { return s_full + 24 + 8u * b; };
-    const uint32_t dq_full = s_full + 40;
-    const uint32_t dq_empty = s_full + 48;
-    const uint32_t dkv_full = s_full + 56;
-    const uint32_t mma_done = s_full + 64;
+    auto qdo_empty = [&](int st) { return bars + 8u * (1 + NST + st); };
+    const uint32_t b0 = bars + 8u * (1 + 2 * NST);
+    auto s_full = [&](int b) { return b0 + 8u * b; };  // one per S buffer
+    const uint32_t dp_full = b0 + 16;
+    const uint32_t p_full = b0 + 24;
+    auto ds_empty = [&](int b) { return b0 + 32 + 8u * b; };
+    const uint32_t dq_full = b0 + 48;
+    const uint32_t dq_empty = b0 + 56;
+    const uint32_t dkv_full = b0 + 64;
+    const uint32_t mma_done = b0 + 72;
+    const uint32_t p_free = b0 + 80;  // single-S layout: P region free again (dV done)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
     const Ctl ctl{abort_flag, p.timeout_ns};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T;
-    const int kt = blockIdx.x / p.BH, bh = blockIdx.x % p.BH;  // heavy key tiles (small kt) first
+    // head-major order: the key tiles of one head run together (their Q, dO
+    // and dQ accumulator stay in L2); within a head, heavy key tiles first
+    const int bh = blockIdx.x / p.n_kt, kt = blockIdx.x % p.n_kt;
     const int q_begin = bwd_q_begin(T, CAUSAL, kt, BM), q_end = bwd_q_end(T, BM);
     const int n_it = q_end - q_begin;
 
     if (tid == 0) {
         mbar_init(kv_full, 1);
-        for (int st = 0; st < C::kStages; ++st) {
+        for (int st = 0; st < NST; ++st) {
             mbar_init(qdo_full(st), 1);
             mbar_init(qdo_empty(st), 1);
         }
-        mbar_init(s_full, 1);
+        mbar_init(s_full(0), 1);
+        mbar_init(s_full(1), 1);
         mbar_init(dp_full, 1);
         mbar_init(p_full, 8);
         mbar_init(ds_empty(0), 1);
@@ -232,6 +275,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(dq_empty, 4);
         mbar_init(dkv_full, 1);
         mbar_init(mma_done, 1);
+        mbar_init(p_free, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -256,8 +300,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d_hint(sV + a * 128 * 128, &tm_v, kv_full, 64 * a, kt * kBN, bh, pol_kv);
             }
             for (int it = 0; it < n_it; ++it) {
-                const int st = it % C::kStages;
-                if (!wait_bar(qdo_empty(st), ((it / C::kStages) & 1) ^ 1, ctl)) break;
+                const int st = it % NST;
+                if (!wait_bar(qdo_empty(st), ((it / NST) & 1) ^ 1, ctl)) break;
                 const int qt = q_begin + it;
                 const uint32_t fb = qdo_full(st);
                 mbar_arrive_expect_tx(fb, 2 * C::kQBytes + 2 * BM * 4);
@@ -274,72 +318,127 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             volatile int never = 0;
             Ctl drain{&never, 100000000ull};
             wait_bar(kv_full, 0, drain);
-            for (uint32_t f = armed > C::kStages ? armed - C::kStages : 0; f < armed; ++f)
-                wait_bar(qdo_full(f % C::kStages), (f / C::kStages) & 1, drain);
+            for (uint32_t f = armed > NST ? armed - NST : 0; f < armed; ++f)
+                wait_bar(qdo_full(f % NST), (f / NST) & 1, drain);
         }
     } else if (warp == 13) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            auto issue_sdp = [&](int st) {
-                // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = BM, K = D (both K-major)
+            // Descriptors are built once; a stage / buffer / k-step is an offset in 16-byte units.
+            const SDesc dK_km = sdesc_make(sK, 16, 1024), dV_km = sdesc_make(sV, 16, 1024);
+            const SDesc dK_mn = sdesc_make(sK, 128 * 128, 1024);
+            const SDesc dQ_km = sdesc_make(sQ(0), 16, 1024), dO_km = sdesc_make(sdO(0), 16, 1024);
+            const SDesc dQ_mn = sdesc_make(sQ(0), BM * 128, 1024), dO_mn = sdesc_make(sdO(0), BM * 128, 1024);
+            const SDesc dS_km = sdesc_make(sDS(0), 16, 1024), dS_mn = sdesc_make(sDS(0), 128 * 128, 1024);
+            constexpr uint32_t kStage16 = C::kStageBytes >> 4, kDS16 = C::kDSBytes >> 4;
+            // S^T = K Q^T into S buffer b: M = 128 keys, N = BM, K = D (both K-major)
+            auto issue_s = [&](int st, int b) {
+                const uint32_t so = st * kStage16;
 #pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t offk = (s >> 2) * (128 * 128) + (s & 3) * 32;
-                    const uint32_t offq = (s >> 2) * (BM * 128) + (s & 3) * 32;
-                    mma_ss(tmem + C::kS, sdesc_sw128(sK + offk, 16, 1024), sdesc_sw128(sQ(st) + offq, 16, 1024),
-                           C::kIdescS, s > 0);
-                }
-                mma_commit(s_full);
+                for (int s = 0; s < D / 16; ++s)
+                    mma_ss_d(tmem + C::kS + b * BM, dK_km, ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4, dQ_km,
+                             so + (((s >> 2) * (BM * 128) + (s & 3) * 32) >> 4), C::kIdescS, s > 0);
+                mma_commit(s_full(b));
+            };
+            // dP^T = V dO^T
+            auto issue_dp = [&](int st) {
+                const uint32_t so = st * kStage16;
 #pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t offk = (s >> 2) * (128 * 128) + (s & 3) * 32;
-                    const uint32_t offq = (s >> 2) * (BM * 128) + (s & 3) * 32;
-                    mma_ss(tmem + C::kDP, sdesc_sw128(sV + offk, 16, 1024), sdesc_sw128(sdO(st) + offq, 16, 1024),
-                           C::kIdescS, s > 0);
-                }
+                for (int s = 0; s < D / 16; ++s)
+                    mma_ss_d(tmem + C::kDP, dV_km, ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4, dO_km,
+                             so + (((s >> 2) * (BM * 128) + (s & 3) * 32) >> 4), C::kIdescS, s > 0);
                 mma_commit(dp_full);
+            };
+            // dV += P^T dO: A = P^T from TMEM, B = dO (MN-major: rows = queries = K)
+            auto issue_dv = [&](int st, int b, int it) {
+                const uint32_t pcol = C::kSDouble ? (C::kS + b * BM + BM / 4) : C::kP;
+                const uint32_t so = st * kStage16;
+#pragma unroll
+                for (int s = 0; s < BM / 16; ++s)
+                    mma_ts_d(tmem + C::kDV, tmem + pcol + s * 8, dO_mn, so + s * (2048 >> 4), C::kIdescDKV,
+                             (it > 0 || s > 0) ? 1u : 0u);
+            };
+            // dK += dS^T Q: A = dS^T (K-major over queries), B = Q (MN-major)
+            auto issue_dk = [&](int st, int b, int it) {
+                const uint32_t so = st * kStage16, bo = b * kDS16;
+#pragma unroll
+                for (int s = 0; s < BM / 16; ++s)
+                    mma_ss_d(tmem + C::kDK, dS_km, bo + (((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4), dQ_mn,
+                             so + s * (2048 >> 4), C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
+            };
+            // dQ tile over the 128 keys: both operands MN-major, K = keys
+            auto issue_dq = [&](int b) {
+                const uint32_t bo = b * kDS16;
+#pragma unroll
+                for (int s = 0; s < 128 / 16; ++s) {
+                    if constexpr (C::kDqT)  // dQ^T [D][BM] = K^T dS^T
+                        mma_ss_d(tmem + C::kDQ, dK_mn, s * (2048 >> 4), dS_mn, bo + s * (2048 >> 4), C::kIdescDQ, s > 0);
+                    else  // dQ [BM][D] = dS K
+                        mma_ss_d(tmem + C::kDQ, dS_mn, bo + s * (2048 >> 4), dK_mn, s * (2048 >> 4), C::kIdescDQ, s > 0);
+                }
+                mma_commit(dq_full);
             };
             if (!wait_bar(kv_full, 0, ctl)) goto mma_teardown;
             if (!wait_bar(qdo_full(0), 0, ctl)) goto mma_teardown;
             tc_fence_after();
-            issue_sdp(0);
+            issue_s(0, 0);
+            issue_dp(0);
+            if constexpr (C::kSDouble) {
+                if (n_it > 1) {
+                    if (!wait_bar(qdo_full(1 % NST), (1 / NST) & 1, ctl)) goto mma_teardown;
+                    tc_fence_after();
+                    issue_s(1 % NST, 1);
+                }
+            }
             for (int it = 0; it < n_it; ++it) {
-                const int st = it % C::kStages, b = it & 1;
-                if (!wait_bar(p_full, it & 1, ctl)) goto mma_teardown;
+                const int st = it % NST, b = it & 1;
+                if (!wait_bar<kCritSleep>(p_full, it & 1, ctl)) goto mma_teardown;
+                FA_TRACE_EVENT(0, it);
                 tc_fence_after();
-                // dV += P^T dO: A = P^T from TMEM, B = dO (MN-major: rows = queries = K)
-#pragma unroll
-                for (int s = 0; s < BM / 16; ++s)
-                    mma_ts(tmem + C::kDV, tmem + C::kP + s * 8, sdesc_sw128(sdO(st) + s * 2048, BM * 128, 1024),
-                           C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
-                if (it + 1 < n_it) {
-                    const int st1 = (it + 1) % C::kStages;
-                    if (!wait_bar(qdo_full(st1), ((it + 1) / C::kStages) & 1, ctl)) goto mma_teardown;
-                    tc_fence_after();
-                    issue_sdp(st1);
+                if constexpr (C::kSDouble) {
+                    // S(it+1) is already in the other buffer; refill dP, then finish tile it
+                    if (it + 1 < n_it) issue_dp((it + 1) % NST);
+                    issue_dv(st, b, it);
+                    issue_dk(st, b, it);
+                    if (it > 0) {
+                        if (!wait_bar<kCritSleep>(dq_empty, (it - 1) & 1, ctl)) goto mma_teardown;
+                        tc_fence_after();
+                    }
+                    FA_TRACE_EVENT(1, it);
+                    issue_dq(b);
+                    FA_TRACE_EVENT(10, it);
+                    mma_commit(qdo_empty(st));
+                    mma_commit(ds_empty(b));
+                    // S(it+2) overwrites buffer b: S(it) was read by the compute warps and
+                    // P(it), aliased there, was read by dV(it), issued above
+                    if (it + 2 < n_it) {
+                        const int st2 = (it + 2) % NST;
+                        if (!wait_bar<kCritSleep>(qdo_full(st2), ((it + 2) / NST) & 1, ctl)) goto mma_teardown;
+                        FA_TRACE_EVENT(11, it);
+                        tc_fence_after();
+                        issue_s(st2, b);
+                    }
+                    FA_TRACE_EVENT(2, it);
+                } else {
+                    // single S buffer (compute(it) has read it): S and dP of it+1 first
+                    if (it + 1 < n_it) {
+                        const int st1 = (it + 1) % NST;
+                        if (!wait_bar<kCritSleep>(qdo_full(st1), ((it + 1) / NST) & 1, ctl)) goto mma_teardown;
+                        tc_fence_after();
+                        issue_s(st1, 0);
+                        issue_dp(st1);
+                    }
+                    issue_dv(st, b, it);
+                    mma_commit(p_free);
+                    issue_dk(st, b, it);
+                    if (it > 0) {
+                        if (!wait_bar<kCritSleep>(dq_empty, (it - 1) & 1, ctl)) goto mma_teardown;
+                        tc_fence_after();
+                    }
+                    issue_dq(b);
+                    mma_commit(qdo_empty(st));
+                    mma_commit(ds_empty(b));
                 }
-                // dK += dS^T Q: A = dS^T (K-major over queries), B = Q (MN-major)
-#pragma unroll
-                for (int s = 0; s < BM / 16; ++s)
-                    mma_ss(tmem + C::kDK, sdesc_sw128(sDS(b) + (s >> 2) * (128 * 128) + (s & 3) * 32, 16, 1024),
-                           sdesc_sw128(sQ(st) + s * 2048, BM * 128, 1024), C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
-                if (it > 0) {
-                    if (!wait_bar(dq_empty, (it - 1) & 1, ctl)) goto mma_teardown;
-                    tc_fence_after();
-                }
-                // dQ tile over the 128 keys: both operands MN-major, K = keys
-#pragma unroll
-                for (int s = 0; s < 128 / 16; ++s) {
-                    if constexpr (C::kDqT)  // dQ^T [D][BM] = K^T dS^T
-                        mma_ss(tmem + C::kDQ, sdesc_sw128(sK + s * 2048, 128 * 128, 1024),
-                               sdesc_sw128(sDS(b) + s * 2048, 128 * 128, 1024), C::kIdescDQ, s > 0);
-                    else  // dQ [BM][D] = dS K
-                        mma_ss(tmem + C::kDQ, sdesc_sw128(sDS(b) + s * 2048, 128 * 128, 1024),
-                               sdesc_sw128(sK + s * 2048, 128 * 128, 1024), C::kIdescDQ, s > 0);
-                }
-                mma_commit(dq_full);
-                mma_commit(qdo_empty(st));
-                mma_commit(ds_empty(b));
             }
             mma_commit(dkv_full);
         mma_teardown:
@@ -353,43 +452,70 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int h = warp >> 2, wq = warp & 3;
         const int key = kt * kBN + 32 * wq + lane;
         const uint32_t lane_base = tmem + ((32u * wq) << 16);
-        const float eff = p.sl2_eff;
+        const float eff = p.sl2_eff, sl2 = p.sl2;
+        const bool prescale = p.prescale != 0;
+        constexpr int NCH = C::kHalf / 32;  // 32-column chunks per thread
         for (int it = 0; it < n_it; ++it) {
-            const int st = it % C::kStages, b = it & 1;
+            const int st = it % NST, b = it & 1;
+            const int sb = C::kSDouble ? b : 0;
             const int qt = q_begin + it, q0 = qt * BM;
             const bool masked = bwd_tile_class(T, CAUSAL, BM, qt, kt) == kMasked;
-            if (!warp_wait(qdo_full(st), (it / C::kStages) & 1, ctl)) break;
-            if (!warp_wait(s_full, it & 1, ctl)) break;
+            if (!warp_wait(qdo_full(st), (it / NST) & 1, ctl)) break;
+            if (!warp_wait<kCritSleep>(s_full(sb), C::kSDouble ? ((it >> 1) & 1) : (it & 1), ctl)) break;
+            if (warp == 0 && lane == 0) FA_TRACE_EVENT(3, it);
+            if (lane == 0) FA_TRACE_EVENT(18 + warp, it);
             tc_fence_after();
-            const float* lse2 = reinterpret_cast<const float*>(smem + (sLse(st) - sbase));
-            const float* dvv = reinterpret_cast<const float*>(smem + (sDv(st) - sbase));
-            float pf[C::kHalf];
+            const float4* lse4 = reinterpret_cast<const float4*>(smem + (sLse(st) - sbase));
+            const float4* dv4 = reinterpret_cast<const float4*>(smem + (sDv(st) - sbase));
+            // P^T for all of this thread's columns (S fully read before P is written over it)
+            uint32_t sr[C::kHalf];
 #pragma unroll
-            for (int ch = 0; ch < C::kHalf / 32; ++ch) {
-                const int c0 = h * C::kHalf + 32 * ch;  // first query column of this chunk
-                uint32_t sr[32];
-                tmem_ld32(lane_base + C::kS + c0, sr);
-                tmem_ld_wait();
-                reg_fence32(sr);
-                uint32_t pk[16];
+            for (int ch = 0; ch < NCH; ++ch)
+                tmem_ld32(lane_base + C::kS + sb * BM + h * C::kHalf + 32 * ch, sr + 32 * ch);
+            tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float s = __uint_as_float(sr[e]);
-                    if (p.prescale) s *= p.sl2;
-                    float pv = ex2_approx(fmaf(s, eff, -lse2[c0 + e]));
-                    if (masked && !bwd_elem_visible(T, CAUSAL, q0 + c0 + e, key)) pv = 0.f;
-                    pf[32 * ch + e] = pv;
-                }
+            for (int ch = 0; ch < NCH; ++ch) reg_fence32(sr + 32 * ch);
+            float* pf = reinterpret_cast<float*>(sr);
+            if (prescale) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]);
-                tmem_st16(lane_base + C::kP + c0 / 2, pk);
+                for (int e = 0; e < C::kHalf; ++e) pf[e] *= sl2;
             }
-            if (!warp_wait(dp_full, it & 1, ctl)) break;
+#pragma unroll
+            for (int e4 = 0; e4 < C::kHalf / 4; ++e4) {
+                const float4 l4 = lse4[(h * C::kHalf) / 4 + e4];
+                pf[4 * e4 + 0] = ex2_approx(fmaf(pf[4 * e4 + 0], eff, -l4.x));
+                pf[4 * e4 + 1] = ex2_approx(fmaf(pf[4 * e4 + 1], eff, -l4.y));
+                pf[4 * e4 + 2] = ex2_approx(fmaf(pf[4 * e4 + 2], eff, -l4.z));
+                pf[4 * e4 + 3] = ex2_approx(fmaf(pf[4 * e4 + 3], eff, -l4.w));
+            }
+            if (masked) {
+#pragma unroll
+                for (int e = 0; e < C::kHalf; ++e)
+                    if (!bwd_elem_visible(T, CAUSAL, q0 + h * C::kHalf + e, key)) pf[e] = 0.f;
+            }
+            {
+                uint32_t pk[C::kHalf / 2];
+#pragma unroll
+                for (int e = 0; e < C::kHalf / 2; ++e) pk[e] = pack_bf16x2(pf[2 * e], pf[2 * e + 1]);
+                if constexpr (!C::kSDouble) {
+                    // P has its own region; dV(it-1) must have read the previous P
+                    if (it > 0 && !warp_wait(p_free, (it - 1) & 1, ctl)) break;
+                }
+                const uint32_t pcol =
+                    C::kSDouble ? (C::kS + sb * BM + BM / 4 + h * C::kHalf / 2) : (C::kP + h * C::kHalf / 2);
+#pragma unroll
+                for (int c = 0; c < C::kHalf / 32; ++c) tmem_st16(lane_base + pcol + 16 * c, pk + 16 * c);
+            }
+            if (warp == 0 && lane == 0) FA_TRACE_EVENT(4, it);
+            if (!warp_wait<kCritSleep>(dp_full, it & 1, ctl)) break;
+            if (warp == 0 && lane == 0) FA_TRACE_EVENT(5, it);
+            if (lane == 0 && warp == 1) FA_TRACE_EVENT(26, it);
+            if (lane == 0 && warp == 5) FA_TRACE_EVENT(27, it);
             if (!warp_wait(ds_empty(b), ((it >> 1) & 1) ^ 1, ctl)) break;
             tc_fence_after();
             const uint32_t ds_base = sDS(b);
 #pragma unroll
-            for (int ch = 0; ch < C::kHalf / 32; ++ch) {
+            for (int ch = 0; ch < NCH; ++ch) {
                 const int c0 = h * C::kHalf + 32 * ch;
                 uint32_t dr[32];
                 tmem_ld32(lane_base + C::kDP + c0, dr);
@@ -398,12 +524,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dS^T row `key`, query columns c0 .. c0+31 -> 4 chunks of 8 in the swizzled tile
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
+                    const float4 da = dv4[(c0 + 8 * g) / 4], db = dv4[(c0 + 8 * g) / 4 + 1];
+                    const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
                     uint32_t w4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int c = 8 * g + 2 * e;
-                        const float d0 = pf[32 * ch + c] * (__uint_as_float(dr[c]) - dvv[c0 + c]);
-                        const float d1 = pf[32 * ch + c + 1] * (__uint_as_float(dr[c + 1]) - dvv[c0 + c + 1]);
+                        const float d0 = pf[32 * ch + c] * (__uint_as_float(dr[c]) - dd[2 * e]);
+                        const float d1 = pf[32 * ch + c + 1] * (__uint_as_float(dr[c + 1]) - dd[2 * e + 1]);
                         w4[e] = pack_bf16x2(d0, d1);
                     }
                     const int col = c0 + 8 * g;
@@ -415,6 +543,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
+            if (lane == 0) FA_TRACE_EVENT(6 + (warp == 0 ? 0 : 0), it);
+            if (lane == 0 && warp > 0) FA_TRACE_EVENT(12 + warp - 1, it);
+            if (warp == 7 && lane == 0) FA_TRACE_EVENT(9, it);
             if (lane == 0) mbar_arrive(p_full);
         }
     } else {
@@ -429,33 +560,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ok = false;
                 break;
             }
+            if (warp == 8 && lane == 0) FA_TRACE_EVENT(7, it);
             tc_fence_after();
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + C::kDQ + 32 * ch, v);
-                tmem_ld_wait();
-                reg_fence32(v);
-                if constexpr (C::kDqT) {
-                    // lane = d; columns = queries q0 + 32 ch + e
-                    float* base = p.dqacc + (static_cast<size_t>(bh) * T + q0 + 32 * ch) * D + r;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (q0 + 32 * ch + e < T) atomicAdd(base + static_cast<size_t>(e) * D, __uint_as_float(v[e]));
-                } else {
-                    // lane = query row q0 + r; columns = d
-                    if (q0 + r < T) {
-                        float* base = p.dqacc + (static_cast<size_t>(bh) * T + q0 + r) * D + 32 * ch;
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            red_add_v4_f32(base + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                           __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                    }
-                }
-            }
+            uint32_t v[64];
+            tmem_ld32(lane_base + C::kDQ, v);
+            tmem_ld32(lane_base + C::kDQ + 32, v + 32);
+            tmem_ld_wait();
+            reg_fence32(v);
+            reg_fence32(v + 32);
+            // the tile is in registers: hand the TMEM columns back before the reductions
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dq_empty);
+            if constexpr (C::kDqT) {
+                // lane = d; columns = queries q0 .. q0+63
+                float* base = p.dqacc + (static_cast<size_t>(bh) * T + q0) * D + r;
+                if (q0 + 64 <= T) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) atomicAdd(base + static_cast<size_t>(e) * D, __uint_as_float(v[e]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (q0 + e < T) atomicAdd(base + static_cast<size_t>(e) * D, __uint_as_float(v[e]));
+                }
+            } else {
+                // lane = query row q0 + r; columns = d
+                if (q0 + r < T) {
+                    float* base = p.dqacc + (static_cast<size_t>(bh) * T + q0 + r) * D;
+#pragma unroll
+                    for (int e = 0; e < 64; e += 4)
+                        red_add_v4_f32(base + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                       __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                }
+            }
+            if (warp == 8 && lane == 0) FA_TRACE_EVENT(8, it);
         }
         if (ok && warp_wait(dkv_full, 0, ctl)) {
             tc_fence_after();
@@ -682,6 +820,13 @@ int launch_bwd_noalloc(const void* q, const void* k, const void* v, const void* 
     fa_bwd_dq_kernel<<<g, 256, 0, stream>>>(dqacc, static_cast<__nv_bfloat16*>(dq), n8, scale);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
+
+#ifdef FA_TRACE
+// Copies the trace of the last traced launch (kTraceSlots x kTraceLen cycle stamps).
+extern "C" int fa_trace_read(unsigned long long* host) {
+    return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -5;
+}
+#endif
 
 int bwd_take_status() {
     int h = 0, z = 0;

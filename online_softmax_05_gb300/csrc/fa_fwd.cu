@@ -38,6 +38,13 @@ static __device__ int g_status_fwd;
 
 namespace {
 
+#ifndef FA_CRIT_SLEEP
+#define FA_CRIT_SLEEP 0
+#endif
+// Waits on the MMA <-> softmax critical path poll back to back unless built
+// with FA_CRIT_SLEEP=1; every other wait lets the hardware park the thread.
+constexpr bool kCritSleep = FA_CRIT_SLEEP != 0;
+
 constexpr int kFwdThreads = 320;
 constexpr float kRescaleThreshold = 0.0f;  // log2 units; see the rescale policy above
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -78,12 +85,15 @@ struct Ctl {
     unsigned long long timeout_ns;
 };
 
-// Bounded wait: true when the phase completed, false when the CTA aborted
-// (this wait ran out of time, or another role already gave up).
+// Slow path of a bounded wait.  kSleep: the hardware suspends the polling
+// thread between checks (for waits off the critical path, so that polling
+// does not take issue slots from busy warps on the same sub-partition);
+// otherwise the thread polls back to back (lowest wake-up latency).
+template <bool kSleep>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
     uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (kSleep ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
         if (*c.abort) return false;
         if (globaltimer_ns() - t0 > c.timeout_ns) {
             *c.abort = 1;
@@ -92,14 +102,18 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
         }
     }
 }
+// Bounded wait: true when the phase completed, false when the CTA aborted
+// (this wait ran out of time, or another role already gave up).
+template <bool kSleep = true>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl c) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, c);
+    return wait_slow<kSleep>(bar, parity, c);
 }
 // Warp-uniform wait: lane 0 polls, the result is broadcast.
+template <bool kSleep = true>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, c);
+    if ((threadIdx.x & 31) == 0) ok = wait_bar<kSleep>(bar, parity, c);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -226,21 +240,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t kv_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
+            // Descriptors are built once; a tile / slot / k-step is an offset in 16-byte units.
+            const SDesc dQ_km = sdesc_make(sQ[0], 16, 1024);
+            const SDesc dKV_km = sdesc_make(sKV, 16, 1024);
+            const SDesc dKV_mn = sdesc_make(sKV, C::kAtomBytes, 1024);
+            constexpr uint32_t kTile16 = C::kTileBytes >> 4;
             auto issue_s = [&](int t, uint32_t slot) {
-                const uint32_t qa = sQ[t], ka = sKV + slot * C::kTileBytes;
+                const uint32_t qo = t * kTile16, ko = slot * kTile16;
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t off = (s >> 2) * C::kAtomBytes + (s & 3) * 32;
-                    mma_ss(tmem + C::kS(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                           C::kIdescS, s > 0);
+                    const uint32_t off = ((s >> 2) * C::kAtomBytes + (s & 3) * 32) >> 4;
+                    mma_ss_d(tmem + C::kS(t), dQ_km, qo + off, dKV_km, ko + off, C::kIdescS, s > 0);
                 }
             };
             auto issue_pv = [&](int t, uint32_t slot, bool acc) {
-                const uint32_t va = sKV + slot * C::kTileBytes;
+                const uint32_t vo = slot * kTile16;
 #pragma unroll
                 for (int s = 0; s < kBN / 16; ++s)
-                    mma_ts(tmem + C::kO(t), tmem + C::kS(t) + s * 8, sdesc_sw128(va + s * 2048, C::kAtomBytes, 1024),
-                           C::kIdescPV, (acc || s > 0) ? 1u : 0u);
+                    mma_ts_d(tmem + C::kO(t), tmem + C::kS(t) + s * 8, dKV_mn, vo + s * (2048 >> 4), C::kIdescPV,
+                             (acc || s > 0) ? 1u : 0u);
             };
             for (int k = 0;; ++k) {
                 int w = item_of(k, p.n_items);
@@ -259,7 +277,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 {
                     const uint32_t ks = kv_cnt % C::kStages;
-                    if (!wait_bar(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                    if (!wait_bar<kCritSleep>(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                     ++kv_cnt;
                     tc_fence_after();
                     issue_s(0, ks);
@@ -272,7 +290,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 for (int j = 0; j < nmax; ++j) {
                     const uint32_t vs = kv_cnt % C::kStages;
-                    if (!wait_bar(kv_full(vs), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                    if (!wait_bar<kCritSleep>(kv_full(vs), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                     ++kv_cnt;
                     tc_fence_after();
                     const bool has_next = j + 1 < nmax;
@@ -281,13 +299,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int t = 0; t < 2; ++t) {
                         const int n = t ? n1 : n0;
                         if (j >= n) continue;
-                        if (!wait_bar(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
+                        if (!wait_bar<kCritSleep>(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
                         ++p_cnt[t];
                         tc_fence_after();
                         issue_pv(t, vs, j > 0);
                         if (j + 1 < n) {
                             if (!k_ready) {
-                                if (!wait_bar(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                                if (!wait_bar<kCritSleep>(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                                 tc_fence_after();
                                 k_ready = true;
                             }
@@ -300,7 +318,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     mma_commit(kv_empty(vs));
                     if (has_next) {
                         if (!k_ready) {
-                            if (!wait_bar(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                            if (!wait_bar<kCritSleep>(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                         }
                         mma_commit(kv_empty(ks));
                         ++kv_cnt;
@@ -333,7 +351,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int n = fwd_num_kv_tiles(T, CAUSAL, tile);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
-                if (!warp_wait(s_full(t), s_cnt & 1, ctl)) goto softmax_done;
+                if (!warp_wait<kCritSleep>(s_full(t), s_cnt & 1, ctl)) goto softmax_done;
                 ++s_cnt;
                 tc_fence_after();
                 uint32_t sr[128];
@@ -353,10 +371,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int c = 0; c < 128; ++c)
                         if (!elem_visible(T, CAUSAL, row, key0 + c)) s[c] = -INFINITY;
                 }
-                float mx = s[0];
+                // row max as a tree: 8 independent chains, then 3 levels
+                float mx8[8];
 #pragma unroll
-                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-                const float m_tile = mx * eff;
+                for (int c = 0; c < 8; ++c) mx8[c] = s[c];
+#pragma unroll
+                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+#pragma unroll
+                for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+                    for (int c = 0; c < w; ++c) mx8[c] = fmaxf(mx8[c], mx8[c + w]);
+                const float m_tile = mx8[0] * eff;
                 const float m_new = fmaxf(m_used, m_tile);
                 float alpha = 1.f;
                 bool need = false;
@@ -369,15 +394,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     l *= alpha;
                 }
                 const float neg = -m_used;
-                float lp = 0.f;
+                float lp8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float p0 = ex2_approx(fmaf(s[2 * c], eff, neg));
                     const float p1 = ex2_approx(fmaf(s[2 * c + 1], eff, neg));
-                    lp += p0 + p1;
+                    lp8[c & 7] += p0 + p1;
                     sr[c] = pack_bf16x2(p0, p1);
                 }
-                l += lp;
+#pragma unroll
+                for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+                    for (int c = 0; c < w; ++c) lp8[c] += lp8[c + w];
+                l += lp8[0];
                 tmem_st32(tS, sr);
                 tmem_st32(tS + 32, sr + 32);
                 // O already holds PV(j-1) (S(j) was committed after it); rescale it

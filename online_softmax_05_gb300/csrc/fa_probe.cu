@@ -171,10 +171,100 @@ __global__ void __launch_bounds__(128, 1)
         for (int i = threadIdx.x; i < bytes; i += blockDim.x) dst[i] = smem[i];
 }
 
+// Issue-rate probe: one thread issues `n` back-to-back 128xNx16 bf16 MMAs
+// (SS, K-major) into one accumulator; cycles to issue them and until the
+// commit lands are written to out[0], out[1].  mode 0: descriptors built per
+// MMA from the shared address; mode 1: descriptors precomputed, 64-bit add
+// per step; mode 2: as mode 1, then the latency of a try_wait on an
+// already completed mbarrier phase is written to out[2].  Operand contents
+// are whatever shared memory holds (not checked).
+__global__ void __launch_bounds__(128, 1) probe_mma_rate_kernel(int N, int n, int mode, long long* out, int* err) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint32_t sA = smem_u32(smem);
+    uint32_t sB = sA + 128 * 64 * 2;
+    uint32_t bar = sB + 256 * 64 * 2;
+    uint32_t tslot = bar + 8;
+    int tid = threadIdx.x, warp = tid >> 5;
+    for (int i = tid; i < (128 + 256) * 64 * 2 / 4; i += 128) reinterpret_cast<uint32_t*>(smem)[i] = 0x3f803f80u;
+    if (warp == 0) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init(bar + 16, 1);
+        fence_mbar_init();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tslot - sA));
+    if (tid == 0) {
+        mbar_arrive(bar + 16);
+        const uint32_t idesc = idesc_bf16_f32(128, N, false, false);
+        long long t0 = clock64();
+        if (mode == 0) {
+            for (int i = 0; i < n; ++i) {
+                const int s = i & 3;
+                mma_ss(tmem, sdesc_sw128(sA + s * 32, 16, 1024), sdesc_sw128(sB + s * 32, 16, 1024), idesc, i > 0);
+            }
+        } else {
+            const uint64_t da = sdesc_sw128(sA, 16, 1024), db = sdesc_sw128(sB, 16, 1024);
+            for (int i = 0; i < n; ++i) {
+                const uint64_t off = static_cast<uint64_t>((i & 3) * 2);
+                mma_ss(tmem, da + off, db + off, idesc, i > 0);
+            }
+        }
+        long long t1 = clock64();
+        long long t3 = 0;
+        if (mode == 2) {
+            // latency of waiting on an mbarrier phase that completed before the MMAs were issued
+            const uint32_t bar2 = bar + 16;
+            const bool ok = mbar_try_wait(bar2, 0);
+            t3 = clock64() - t1;
+            if (!ok) atomicExch(err, 2);
+        }
+        mma_commit(bar);
+        probe_wait(bar, 0, err);
+        long long t2 = clock64();
+        out[0] = t1 - t0;
+        out[1] = t2 - t0;
+        out[2] = t3;
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 }  // namespace
 }  // namespace fa
 
 extern "C" {
+
+int probe_mma_rate(int N, int n, int mode, long long* out_host) {
+    if (!(N == 64 || N == 128 || N == 256) || n < 1 || n > 4096) return -1;
+    int* err = nullptr;
+    long long* out = nullptr;
+    if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) return -5;
+    if (cudaMalloc(&out, 3 * sizeof(long long)) != cudaSuccess) return -5;
+    cudaMemset(err, 0, sizeof(int));
+    int smem = 1024 + (128 + 256) * 64 * 2 + 64;
+    if (mode < 0 || mode > 2) return -1;
+    cudaFuncSetAttribute(fa::probe_mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    fa::probe_mma_rate_kernel<<<1, 128, smem>>>(N, n, mode, out, err);
+    cudaError_t e = cudaDeviceSynchronize();
+    int h = 0;
+    cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaMemcpy(out_host, out, 3 * sizeof(long long), cudaMemcpyDeviceToHost);
+    cudaFree(err);
+    cudaFree(out);
+    if (e != cudaSuccess) return -5;
+    return h ? -7 : 0;
+}
+
 
 int probe_mma(int a_mode, int b_mode, int N, int K, const void* A, const void* B, float* out) {
     if (a_mode < 0 || a_mode > 2 || b_mode < 0 || b_mode > 1) return -1;

@@ -47,6 +47,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Same, but a thread whose phase has not completed is suspended by the
+// hardware until it completes or about `hint_ns` elapses (no busy spinning
+// that would take issue slots from the other warps of its sub-partition).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -206,6 +221,40 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
     return d;
+}
+
+// A descriptor split into 32-bit halves.  The start-address field lives in
+// the low word, so stepping through a tile is one 32-bit add of the byte
+// offset >> 4 (no carry: shared addresses and offsets stay below 256 KB).
+struct SDesc {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_make(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    const uint64_t d = sdesc_sw128(saddr, lbo_bytes, sbo_bytes);
+    return SDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+// mma_ss with descriptors a/b advanced by a_off16 / b_off16 (bytes >> 4).
+__device__ __forceinline__ void mma_ss_d(uint32_t d_tmem, SDesc a, uint32_t a_off16, SDesc b, uint32_t b_off16,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo + a_off16), "r"(a.hi), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// mma_ts with the B descriptor advanced by b_off16.
+__device__ __forceinline__ void mma_ts_d(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t b_off16, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D:
