@@ -104,8 +104,8 @@ struct BwdCfg {
 };
 
 struct BwdParams {
-    const float* lse2;   // [BH][T_pad] log2-domain LSE
-    const float* dvec;   // [BH][T_pad] D
+    const float* lse2;   // [BH][T_pad] -LSE * log2(e)
+    const float* dvec;   // [BH][T_pad] -D
     float* dqacc;        // [BH][T][D]
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -153,8 +153,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) 
 }
 
 // ---------------------------------------------------------------- preprocess
-// D_i = rowsum(dO o O) ("Lab 06", section 4), LSE2 = LSE * log2(e); rows
-// t >= T of the padded vectors are 0; dQacc = 0.  8 elements per thread.
+// D_i = rowsum(dO o O) ("Lab 06", section 4) and LSE2 = LSE * log2(e), both
+// stored NEGATED (the main kernel adds them with packed FMAs); rows t >= T
+// of the padded vectors are 0; dQacc = 0.  8 elements per thread.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dO,
@@ -193,8 +194,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
 #pragma unroll
         for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, TPR);
         if (in && sub == 0) {
-            dvec[r] = acc;
-            lse2[r] = (t < T) ? lse[static_cast<size_t>(bh) * T + t] * kLog2e : 0.f;
+            dvec[r] = -acc;
+            lse2[r] = (t < T) ? -lse[static_cast<size_t>(bh) * T + t] * kLog2e : 0.f;
         }
     }
 }
@@ -480,13 +481,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int e = 0; e < C::kHalf; ++e) pf[e] *= sl2;
             }
+            // P^T = exp2(S^T c - LSE2): one packed FMA per pair (the smem vector holds -LSE2)
+            const uint64_t eff2 = f2(eff, eff);
 #pragma unroll
             for (int e4 = 0; e4 < C::kHalf / 4; ++e4) {
                 const float4 l4 = lse4[(h * C::kHalf) / 4 + e4];
-                pf[4 * e4 + 0] = ex2_approx(fmaf(pf[4 * e4 + 0], eff, -l4.x));
-                pf[4 * e4 + 1] = ex2_approx(fmaf(pf[4 * e4 + 1], eff, -l4.y));
-                pf[4 * e4 + 2] = ex2_approx(fmaf(pf[4 * e4 + 2], eff, -l4.z));
-                pf[4 * e4 + 3] = ex2_approx(fmaf(pf[4 * e4 + 3], eff, -l4.w));
+                float x0, x1, x2, x3;
+                f2_split(fma2(f2(pf[4 * e4 + 0], pf[4 * e4 + 1]), eff2, f2(l4.x, l4.y)), x0, x1);
+                f2_split(fma2(f2(pf[4 * e4 + 2], pf[4 * e4 + 3]), eff2, f2(l4.z, l4.w)), x2, x3);
+                pf[4 * e4 + 0] = ex2_approx(x0);
+                pf[4 * e4 + 1] = ex2_approx(x1);
+                pf[4 * e4 + 2] = ex2_approx(x2);
+                pf[4 * e4 + 3] = ex2_approx(x3);
             }
             if (masked) {
 #pragma unroll
@@ -524,14 +530,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dS^T row `key`, query columns c0 .. c0+31 -> 4 chunks of 8 in the swizzled tile
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
+                    // dS^T = P^T o (dP^T - D): packed add of -D, packed multiply
                     const float4 da = dv4[(c0 + 8 * g) / 4], db = dv4[(c0 + 8 * g) / 4 + 1];
-                    const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+                    const uint64_t nd[4] = {f2(da.x, da.y), f2(da.z, da.w), f2(db.x, db.y), f2(db.z, db.w)};
                     uint32_t w4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int c = 8 * g + 2 * e;
-                        const float d0 = pf[32 * ch + c] * (__uint_as_float(dr[c]) - dd[2 * e]);
-                        const float d1 = pf[32 * ch + c + 1] * (__uint_as_float(dr[c + 1]) - dd[2 * e + 1]);
+                        const uint64_t t2 = add2(f2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), nd[e]);
+                        float d0, d1;
+                        f2_split(mul2(f2(pf[32 * ch + c], pf[32 * ch + c + 1]), t2), d0, d1);
                         w4[e] = pack_bf16x2(d0, d1);
                     }
                     const int col = c0 + 8 * g;

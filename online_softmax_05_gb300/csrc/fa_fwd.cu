@@ -36,6 +36,21 @@ namespace fa {
 
 static __device__ int g_status_fwd;
 
+// Optional cycle tracing of one CTA's first work item (build with
+// -DFA_TRACE; off in the library): slot = event kind, index = key tile.
+#ifdef FA_TRACE
+constexpr int kFTraceSlots = 12, kFTraceLen = 128;
+static __device__ unsigned long long g_ftrace[kFTraceSlots][kFTraceLen];
+#define FA_FTRACE(slot, idx)                                                                     \
+    do {                                                                                         \
+        if (blockIdx.x == 0 && k == 0 && (idx) < kFTraceLen) g_ftrace[slot][idx] = clock64();     \
+    } while (0)
+#else
+#define FA_FTRACE(slot, idx) \
+    do {                     \
+    } while (0)
+#endif
+
 namespace {
 
 #ifndef FA_CRIT_SLEEP
@@ -300,6 +315,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         const int n = t ? n1 : n0;
                         if (j >= n) continue;
                         if (!wait_bar<kCritSleep>(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
+                        FA_FTRACE(0 + t, j);
                         ++p_cnt[t];
                         tc_fence_after();
                         issue_pv(t, vs, j > 0);
@@ -314,6 +330,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         } else {
                             mma_commit(o_full(t));
                         }
+                        FA_FTRACE(2 + t, j);
                     }
                     mma_commit(kv_empty(vs));
                     if (has_next) {
@@ -352,6 +369,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
                 if (!warp_wait<kCritSleep>(s_full(t), s_cnt & 1, ctl)) goto softmax_done;
+                if (wq == 0 && lane == 0) FA_FTRACE(4 + t, j);
                 ++s_cnt;
                 tc_fence_after();
                 uint32_t sr[128];
@@ -362,8 +380,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int c = 0; c < 4; ++c) reg_fence32(sr + 32 * c);
                 float* s = reinterpret_cast<float*>(sr);
                 if (p.prescale) {
+                    const uint64_t sl2x2 = f2(p.sl2, p.sl2);
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) s[c] *= p.sl2;
+                    for (int c = 0; c < 64; ++c) {
+                        const uint64_t v = mul2(f2(s[2 * c], s[2 * c + 1]), sl2x2);
+                        f2_split(v, s[2 * c], s[2 * c + 1]);
+                    }
                 }
                 if (fwd_tile_class(T, CAUSAL, tile, j) == kMasked) {
                     const int key0 = j * kBN;
@@ -371,17 +393,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int c = 0; c < 128; ++c)
                         if (!elem_visible(T, CAUSAL, row, key0 + c)) s[c] = -INFINITY;
                 }
-                // row max as a tree: 8 independent chains, then 3 levels
+                // row max: 8 independent chains of 3-input max, then a small tree
                 float mx8[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) mx8[c] = s[c];
+                for (int c = 0; c < 8; ++c) mx8[c] = fmaxf(s[c], s[c + 8]);
 #pragma unroll
-                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                for (int c = 16; c < 128; c += 16)
 #pragma unroll
-                for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-                    for (int c = 0; c < w; ++c) mx8[c] = fmaxf(mx8[c], mx8[c + w]);
-                const float m_tile = mx8[0] * eff;
+                    for (int a = 0; a < 8; ++a) mx8[a] = fmax3(mx8[a], s[c + a], s[c + 8 + a]);
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
+                const float m_tile = mx * eff;
+                if (wq == 0 && lane == 0) FA_FTRACE(6 + t, j);
                 const float m_new = fmaxf(m_used, m_tile);
                 float alpha = 1.f;
                 bool need = false;
@@ -393,20 +416,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     m_used = m_new;
                     l *= alpha;
                 }
-                const float neg = -m_used;
-                float lp8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // P = exp2(S * c - m): packed FMA for the argument, packed add for the row sum
+                const uint64_t eff2 = f2(eff, eff), neg2 = f2(-m_used, -m_used);
+                uint64_t lp2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
-                    const float p0 = ex2_approx(fmaf(s[2 * c], eff, neg));
-                    const float p1 = ex2_approx(fmaf(s[2 * c + 1], eff, neg));
-                    lp8[c & 7] += p0 + p1;
+                    float x0, x1;
+                    f2_split(fma2(f2(s[2 * c], s[2 * c + 1]), eff2, neg2), x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    lp2[c & 3] = add2(lp2[c & 3], f2(p0, p1));
                     sr[c] = pack_bf16x2(p0, p1);
                 }
-#pragma unroll
-                for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-                    for (int c = 0; c < w; ++c) lp8[c] += lp8[c + w];
-                l += lp8[0];
+                {
+                    float a0, a1, b0, b1;
+                    f2_split(add2(add2(lp2[0], lp2[1]), add2(lp2[2], lp2[3])), a0, a1);
+                    (void)b0;
+                    (void)b1;
+                    l += a0 + a1;
+                }
                 tmem_st32(tS, sr);
                 tmem_st32(tS + 32, sr + 32);
                 // O already holds PV(j-1) (S(j) was committed after it); rescale it
@@ -418,8 +445,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         tmem_ld32(tO + 32 * c, orr);
                         tmem_ld_wait();
                         reg_fence32(orr);
+                        const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        for (int e = 0; e < 32; e += 2) {
+                            float o0, o1;
+                            f2_split(mul2(f2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2), o0, o1);
+                            orr[e] = __float_as_uint(o0);
+                            orr[e + 1] = __float_as_uint(o1);
+                        }
                         tmem_st32(tO + 32 * c, orr);
                     }
                 }
@@ -427,6 +460,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(t));
+                if (wq == 0 && lane == 0) FA_FTRACE(8 + t, j);
+                if (wq == 3 && lane == 0) FA_FTRACE(10 + t, j);
             }
             // ---- epilogue: O = acc / l through shared memory and a TMA store; LSE per row
             if (!warp_wait(o_full(t), o_cnt & 1, ctl)) goto softmax_done;
@@ -529,6 +564,12 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     if (dbg.ev[1]) cudaEventRecord(dbg.ev[1], stream);
     return rc;
 }
+
+#ifdef FA_TRACE
+extern "C" int fa_ftrace_read(unsigned long long* host) {
+    return cudaMemcpyFromSymbol(host, g_ftrace, sizeof(g_ftrace)) == cudaSuccess ? 0 : -5;
+}
+#endif
 
 int fwd_take_status() {
     int h = 0, z = 0;

@@ -210,11 +210,44 @@ __global__ void __launch_bounds__(128, 1) probe_mma_rate_kernel(int N, int n, in
                 const int s = i & 3;
                 mma_ss(tmem, sdesc_sw128(sA + s * 32, 16, 1024), sdesc_sw128(sB + s * 32, 16, 1024), idesc, i > 0);
             }
-        } else {
+        } else if (mode <= 2) {
             const uint64_t da = sdesc_sw128(sA, 16, 1024), db = sdesc_sw128(sB, 16, 1024);
             for (int i = 0; i < n; ++i) {
                 const uint64_t off = static_cast<uint64_t>((i & 3) * 2);
                 mma_ss(tmem, da + off, db + off, idesc, i > 0);
+            }
+        } else if (mode >= 8) {
+            // 8: TS B-MN, 9: SS A-MN B-MN, 10: TS B-K, 11: SS K/K -- alternating between two
+            // independent accumulators (columns 0 and 256 - N; two chains in flight)
+            const bool ts = (mode == 8 || mode == 10), amn = (mode == 9), bmn = (mode == 8 || mode == 9);
+            const uint32_t id2 = idesc_bf16_f32(128, N, amn, bmn);
+            const uint64_t da = amn ? sdesc_sw128(sA, 64 * 128, 1024) : sdesc_sw128(sA, 16, 1024);
+            const uint64_t db = bmn ? sdesc_sw128(sB, 64 * 128, 1024) : sdesc_sw128(sB, 16, 1024);
+            const uint32_t acc2 = tmem + 256u;
+            for (int i = 0; i < n; ++i) {
+                const int k = i >> 1;
+                const uint64_t offa = amn ? static_cast<uint64_t>((k & 3) * 128) : static_cast<uint64_t>((k & 3) * 2);
+                const uint64_t offb = bmn ? static_cast<uint64_t>((k & 3) * 128) : static_cast<uint64_t>((k & 3) * 2);
+                const uint32_t d = (i & 1) ? acc2 - (ts ? 0u : 0u) : tmem;
+                if (ts)
+                    mma_ts((i & 1) ? tmem + 128u : tmem, tmem + 384u + (k & 3) * 8, db + offb, id2, i > 1);
+                else
+                    mma_ss((i & 1) ? tmem + 256u : d, da + offa, db + offb, id2, i > 1);
+            }
+        } else {
+            // mode 3: A MN-major, 4: B MN-major, 5: both MN-major, 6: A from TMEM (B K-major),
+            // 7: A from TMEM with B MN-major
+            const bool amn = (mode == 3 || mode == 5), bmn = (mode == 4 || mode == 5 || mode == 7);
+            const uint32_t id2 = idesc_bf16_f32(128, N, amn, bmn);
+            const uint64_t da = amn ? sdesc_sw128(sA, 64 * 128, 1024) : sdesc_sw128(sA, 16, 1024);
+            const uint64_t db = bmn ? sdesc_sw128(sB, 64 * 128, 1024) : sdesc_sw128(sB, 16, 1024);
+            for (int i = 0; i < n; ++i) {
+                const uint64_t offa = amn ? static_cast<uint64_t>((i & 3) * 128) : static_cast<uint64_t>((i & 3) * 2);
+                const uint64_t offb = bmn ? static_cast<uint64_t>((i & 3) * 128) : static_cast<uint64_t>((i & 3) * 2);
+                if (mode >= 6)
+                    mma_ts(tmem, tmem + 256u + (i & 3) * 8, db + offb, id2, i > 0);
+                else
+                    mma_ss(tmem, da + offa, db + offb, id2, i > 0);
             }
         }
         long long t1 = clock64();
@@ -239,10 +272,57 @@ __global__ void __launch_bounds__(128, 1) probe_mma_rate_kernel(int N, int n, in
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Throughput of exp2: mode 0 = ex2.approx (MUFU), mode 1 = polynomial on
+// the FMA/ALU pipes (round-to-nearest by the 1.5*2^23 add, degree-3
+// least-squares fit of 2^f on [-1/2, 1/2], integer add into the exponent).
+// 8 independent chains per thread; cycles for `iters` x 8 evaluations per
+// thread are written to out[warp].
+__device__ __forceinline__ float exp2_poly3(float x) {
+    x = fmaxf(x, -126.f);
+    const float t = x + 12582912.f;  // 1.5 * 2^23: rounds x to an integer in the low mantissa bits
+    const float r = t - 12582912.f;
+    const float f = x - r;             // in [-0.5, 0.5]
+    float p = fmaf(fmaf(fmaf(0.0555041f, f, 0.2402265f), f, 0.6931472f), f, 1.0f);
+    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+__global__ void probe_exp2_rate_kernel(int mode, int iters, float* sink, long long* out) {
+    float v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = -0.001f * (threadIdx.x + c);
+    __syncthreads();
+    long long t0 = clock64();
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = (mode == 0 ? ex2_approx(v[c]) : exp2_poly3(v[c])) - 1.0f;
+    }
+    long long t1 = clock64();
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc += v[c];
+    sink[threadIdx.x] = acc;
+    if ((threadIdx.x & 31) == 0) out[threadIdx.x >> 5] = t1 - t0;
+}
+
 }  // namespace
 }  // namespace fa
 
 extern "C" {
+
+int probe_exp2_rate(int mode, int iters, int warps, long long* out_host, float* max_rel_err) {
+    float* sink = nullptr;
+    long long* out = nullptr;
+    if (warps < 1 || warps > 32) return -1;
+    cudaMalloc(&sink, 1024 * sizeof(float));
+    cudaMalloc(&out, 32 * sizeof(long long));
+    fa::probe_exp2_rate_kernel<<<1, 32 * warps>>>(mode, iters, sink, out);
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaMemcpy(out_host, out, warps * sizeof(long long), cudaMemcpyDeviceToHost);
+    cudaFree(sink);
+    cudaFree(out);
+    (void)max_rel_err;
+    return e == cudaSuccess ? 0 : -5;
+}
+
 
 int probe_mma_rate(int N, int n, int mode, long long* out_host) {
     if (!(N == 64 || N == 128 || N == 256) || n < 1 || n > 4096) return -1;
@@ -252,7 +332,7 @@ int probe_mma_rate(int N, int n, int mode, long long* out_host) {
     if (cudaMalloc(&out, 3 * sizeof(long long)) != cudaSuccess) return -5;
     cudaMemset(err, 0, sizeof(int));
     int smem = 1024 + (128 + 256) * 64 * 2 + 64;
-    if (mode < 0 || mode > 2) return -1;
+    if (mode < 0 || mode > 11) return -1;
     cudaFuncSetAttribute(fa::probe_mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     fa::probe_mma_rate_kernel<<<1, 128, smem>>>(N, n, mode, out, err);
     cudaError_t e = cudaDeviceSynchronize();
