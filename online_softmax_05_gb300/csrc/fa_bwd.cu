@@ -15,8 +15,8 @@
 //                              columns each (TMEM lane = key row)
 //                  warps 8-11  dQ drain (fp32 reductions into the
 //                              accumulator) and the dK/dV epilogue
-//                  warp 12     TMA producer (K, V once; Q, dO, LSE2, D per
-//                              query tile into a 3-stage ring)
+//                  warp 12     TMA producer (K, V once; per query tile Q with
+//                              -LSE2, -D into a 4-stage ring, dO into a 3-stage ring)
 //                  warp 13     tcgen05 issuer
 //                Per query tile: S^T = K Q^T and dP^T = V dO^T into TMEM;
 //                dV += P^T dO with P^T read from TMEM; dK += dS^T Q and the
@@ -76,17 +76,20 @@ struct BwdCfg {
     static constexpr bool kSDouble = (D == 128);
     static constexpr int kKVBytes = 128 * D * 2;     // one K or V tile
     static constexpr int kQBytes = BM * D * 2;       // one Q or dO tile
-    static constexpr int kStages = 3;
-    static constexpr int kStageBytes = ((2 * kQBytes + 2 * BM * 4) + 1023) / 1024 * 1024;
+    // Q (with its -LSE2 and -D vectors) and dO travel in separate rings: S(i+2)
+    // needs Q two tiles ahead while dO is needed one tile ahead.
+    static constexpr int kQStages = 4, kDOStages = 3;
+    static constexpr int kQStageBytes = kQBytes + 1024;  // + -LSE2[BM], -D[BM] (<= 1 KB)
     static constexpr int kDSBytes = 128 * BM * 2;    // dS^T tile [128 keys][BM queries] bf16
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKVBytes;
-    static constexpr int kStageOff = 2 * kKVBytes;
-    static constexpr int kDSOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kQRingOff = 2 * kKVBytes;
+    static constexpr int kDORingOff = kQRingOff + kQStages * kQStageBytes;
+    static constexpr int kDSOff = kDORingOff + kDOStages * kQBytes;
     static constexpr int kBarOff = kDSOff + 2 * kDSBytes;
-    // kv_full, qdo_full[S], qdo_empty[S], s_full[2], dp_full, p_full, ds_empty[2], dq_full, dq_empty,
-    // dkv_full, mma_done, p_free
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 5;
+    // kv_full, q_full[4], q_empty[4], do_full[3], do_empty[3], s_full[2], dp_full, p_full,
+    // ds_empty[2], dq_full, dq_empty, dkv_full, mma_done, p_free
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 2 + 2 + 2 + 5;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -224,21 +227,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        BwdParams p) {
     using C = BwdCfg<D>;
     constexpr int BM = C::BM;
-    constexpr int NST = C::kStages;
+    constexpr int NQS = C::kQStages, NDS = C::kDOStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sK = sbase + C::kKOff, sV = sbase + C::kVOff;
-    auto sQ = [&](int st) { return sbase + C::kStageOff + st * C::kStageBytes; };
-    auto sdO = [&](int st) { return sQ(st) + C::kQBytes; };
-    auto sLse = [&](int st) { return sQ(st) + 2 * C::kQBytes; };
+    auto sQ = [&](int st) { return sbase + C::kQRingOff + st * C::kQStageBytes; };
+    auto sLse = [&](int st) { return sQ(st) + C::kQBytes; };
     auto sDv = [&](int st) { return sLse(st) + BM * 4; };
+    auto sdO = [&](int st) { return sbase + C::kDORingOff + st * C::kQBytes; };
     auto sDS = [&](int b) { return sbase + C::kDSOff + b * C::kDSBytes; };
     const uint32_t bars = sbase + C::kBarOff;
     const uint32_t kv_full = bars;
-    auto qdo_full = [&](int st) { return bars + 8u * (1 + st); };
-    auto qdo_empty = [&](int st) { return bars + 8u * (1 + NST + st); };
-    const uint32_t b0 = bars + 8u * (1 + 2 * NST);
+    auto q_full = [&](int st) { return bars + 8u * (1 + st); };
+    auto q_empty = [&](int st) { return bars + 8u * (1 + NQS + st); };
+    auto do_full = [&](int st) { return bars + 8u * (1 + 2 * NQS + st); };
+    auto do_empty = [&](int st) { return bars + 8u * (1 + 2 * NQS + NDS + st); };
+    const uint32_t b0 = bars + 8u * (1 + 2 * NQS + 2 * NDS);
     auto s_full = [&](int b) { return b0 + 8u * b; };  // one per S buffer
     const uint32_t dp_full = b0 + 16;
     const uint32_t p_full = b0 + 24;
@@ -262,9 +267,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (tid == 0) {
         mbar_init(kv_full, 1);
-        for (int st = 0; st < NST; ++st) {
-            mbar_init(qdo_full(st), 1);
-            mbar_init(qdo_empty(st), 1);
+        for (int st = 0; st < NQS; ++st) {
+            mbar_init(q_full(st), 1);
+            mbar_init(q_empty(st), 1);
+        }
+        for (int st = 0; st < NDS; ++st) {
+            mbar_init(do_full(st), 1);
+            mbar_init(do_empty(st), 1);
         }
         mbar_init(s_full(0), 1);
         mbar_init(s_full(1), 1);
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == 12) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t armed = 0;  // number of Q/dO fills issued
+            uint32_t q_armed = 0, do_armed = 0;  // fills issued per ring
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
             mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
@@ -301,26 +310,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d_hint(sV + a * 128 * 128, &tm_v, kv_full, 64 * a, kt * kBN, bh, pol_kv);
             }
             for (int it = 0; it < n_it; ++it) {
-                const int st = it % NST;
-                if (!wait_bar(qdo_empty(st), ((it / NST) & 1) ^ 1, ctl)) break;
                 const int qt = q_begin + it;
-                const uint32_t fb = qdo_full(st);
-                mbar_arrive_expect_tx(fb, 2 * C::kQBytes + 2 * BM * 4);
-                ++armed;
-                for (int a = 0; a < C::kAtomsD; ++a) {
-                    tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qt * BM, bh, pol_q);
-                    tma_load_3d_hint(sdO(st) + a * BM * 128, &tm_do, fb, 64 * a, qt * BM, bh, pol_q);
+                {   // Q tile with its -LSE2 and -D vectors
+                    const int st = it % NQS;
+                    if (!wait_bar(q_empty(st), ((it / NQS) & 1) ^ 1, ctl)) break;
+                    const uint32_t fb = q_full(st);
+                    mbar_arrive_expect_tx(fb, C::kQBytes + 2 * BM * 4);
+                    ++q_armed;
+                    for (int a = 0; a < C::kAtomsD; ++a)
+                        tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qt * BM, bh, pol_q);
+                    const size_t voff = static_cast<size_t>(bh) * p.T_pad + static_cast<size_t>(qt) * BM;
+                    bulk_load_1d(sLse(st), p.lse2 + voff, BM * 4, fb);
+                    bulk_load_1d(sDv(st), p.dvec + voff, BM * 4, fb);
                 }
-                const size_t voff = static_cast<size_t>(bh) * p.T_pad + static_cast<size_t>(qt) * BM;
-                bulk_load_1d(sLse(st), p.lse2 + voff, BM * 4, fb);
-                bulk_load_1d(sDv(st), p.dvec + voff, BM * 4, fb);
+                {   // dO tile
+                    const int st = it % NDS;
+                    if (!wait_bar(do_empty(st), ((it / NDS) & 1) ^ 1, ctl)) break;
+                    const uint32_t fb = do_full(st);
+                    mbar_arrive_expect_tx(fb, C::kQBytes);
+                    ++do_armed;
+                    for (int a = 0; a < C::kAtomsD; ++a)
+                        tma_load_3d_hint(sdO(st) + a * BM * 128, &tm_do, fb, 64 * a, qt * BM, bh, pol_q);
+                }
             }
             // drain: copies still in flight must land before the CTA exits
             volatile int never = 0;
             Ctl drain{&never, 100000000ull};
             wait_bar(kv_full, 0, drain);
-            for (uint32_t f = armed > NST ? armed - NST : 0; f < armed; ++f)
-                wait_bar(qdo_full(f % NST), (f / NST) & 1, drain);
+            for (uint32_t f = q_armed > NQS ? q_armed - NQS : 0; f < q_armed; ++f)
+                wait_bar(q_full(f % NQS), (f / NQS) & 1, drain);
+            for (uint32_t f = do_armed > NDS ? do_armed - NDS : 0; f < do_armed; ++f)
+                wait_bar(do_full(f % NDS), (f / NDS) & 1, drain);
         }
     } else if (warp == 13) {
         // ------------------------------------------------------------ MMA issuer
@@ -331,10 +351,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const SDesc dQ_km = sdesc_make(sQ(0), 16, 1024), dO_km = sdesc_make(sdO(0), 16, 1024);
             const SDesc dQ_mn = sdesc_make(sQ(0), BM * 128, 1024), dO_mn = sdesc_make(sdO(0), BM * 128, 1024);
             const SDesc dS_km = sdesc_make(sDS(0), 16, 1024), dS_mn = sdesc_make(sDS(0), 128 * 128, 1024);
-            constexpr uint32_t kStage16 = C::kStageBytes >> 4, kDS16 = C::kDSBytes >> 4;
+            constexpr uint32_t kQStage16 = C::kQStageBytes >> 4, kDOStage16 = C::kQBytes >> 4;
+            constexpr uint32_t kDS16 = C::kDSBytes >> 4;
             // S^T = K Q^T into S buffer b: M = 128 keys, N = BM, K = D (both K-major)
             auto issue_s = [&](int st, int b) {
-                const uint32_t so = st * kStage16;
+                const uint32_t so = st * kQStage16;
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s)
                     mma_ss_d(tmem + C::kS + b * BM, dK_km, ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4, dQ_km,
@@ -343,101 +364,117 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             };
             // dP^T = V dO^T
             auto issue_dp = [&](int st) {
-                const uint32_t so = st * kStage16;
+                const uint32_t so = st * kDOStage16;
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s)
                     mma_ss_d(tmem + C::kDP, dV_km, ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4, dO_km,
                              so + (((s >> 2) * (BM * 128) + (s & 3) * 32) >> 4), C::kIdescS, s > 0);
                 mma_commit(dp_full);
             };
-            // dV += P^T dO: A = P^T from TMEM, B = dO (MN-major: rows = queries = K)
-            auto issue_dv = [&](int st, int b, int it) {
+            // One k-step of dV, dK or the dQ tile.  These are transposed-operand (or
+            // TMEM-operand) MMAs: back to back on one accumulator they run slower than
+            // when consecutive instructions alternate between independent accumulators,
+            // so the issue order below interleaves their k-steps.
+            auto step_dv = [&](int st, int b, int it, int s) {
                 const uint32_t pcol = C::kSDouble ? (C::kS + b * BM + BM / 4) : C::kP;
-                const uint32_t so = st * kStage16;
-#pragma unroll
-                for (int s = 0; s < BM / 16; ++s)
-                    mma_ts_d(tmem + C::kDV, tmem + pcol + s * 8, dO_mn, so + s * (2048 >> 4), C::kIdescDKV,
-                             (it > 0 || s > 0) ? 1u : 0u);
+                mma_ts_d(tmem + C::kDV, tmem + pcol + s * 8, dO_mn, st * kDOStage16 + s * (2048 >> 4), C::kIdescDKV,
+                         (it > 0 || s > 0) ? 1u : 0u);
             };
-            // dK += dS^T Q: A = dS^T (K-major over queries), B = Q (MN-major)
-            auto issue_dk = [&](int st, int b, int it) {
-                const uint32_t so = st * kStage16, bo = b * kDS16;
-#pragma unroll
-                for (int s = 0; s < BM / 16; ++s)
-                    mma_ss_d(tmem + C::kDK, dS_km, bo + (((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4), dQ_mn,
-                             so + s * (2048 >> 4), C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
+            auto step_dk = [&](int st, int b, int it, int s) {
+                mma_ss_d(tmem + C::kDK, dS_km, b * kDS16 + (((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4), dQ_mn,
+                         st * kQStage16 + s * (2048 >> 4), C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
             };
-            // dQ tile over the 128 keys: both operands MN-major, K = keys
-            auto issue_dq = [&](int b) {
-                const uint32_t bo = b * kDS16;
-#pragma unroll
-                for (int s = 0; s < 128 / 16; ++s) {
-                    if constexpr (C::kDqT)  // dQ^T [D][BM] = K^T dS^T
-                        mma_ss_d(tmem + C::kDQ, dK_mn, s * (2048 >> 4), dS_mn, bo + s * (2048 >> 4), C::kIdescDQ, s > 0);
-                    else  // dQ [BM][D] = dS K
-                        mma_ss_d(tmem + C::kDQ, dS_mn, bo + s * (2048 >> 4), dK_mn, s * (2048 >> 4), C::kIdescDQ, s > 0);
-                }
-                mma_commit(dq_full);
+            auto step_dq = [&](int b, int s) {
+                if constexpr (C::kDqT)  // dQ^T [D][BM] = K^T dS^T
+                    mma_ss_d(tmem + C::kDQ, dK_mn, s * (2048 >> 4), dS_mn, b * kDS16 + s * (2048 >> 4), C::kIdescDQ,
+                             s > 0);
+                else  // dQ [BM][D] = dS K
+                    mma_ss_d(tmem + C::kDQ, dS_mn, b * kDS16 + s * (2048 >> 4), dK_mn, s * (2048 >> 4), C::kIdescDQ,
+                             s > 0);
             };
+            constexpr int NKV = BM / 16, NQ = 128 / 16;  // k-steps of dV / dK and of the dQ tile
             if (!wait_bar(kv_full, 0, ctl)) goto mma_teardown;
-            if (!wait_bar(qdo_full(0), 0, ctl)) goto mma_teardown;
+            if (!wait_bar(q_full(0), 0, ctl)) goto mma_teardown;
             tc_fence_after();
             issue_s(0, 0);
+            if (!wait_bar(do_full(0), 0, ctl)) goto mma_teardown;
+            tc_fence_after();
             issue_dp(0);
             if constexpr (C::kSDouble) {
                 if (n_it > 1) {
-                    if (!wait_bar(qdo_full(1 % NST), (1 / NST) & 1, ctl)) goto mma_teardown;
+                    if (!wait_bar(q_full(1), 0, ctl)) goto mma_teardown;
                     tc_fence_after();
-                    issue_s(1 % NST, 1);
+                    issue_s(1, 1);
                 }
             }
             for (int it = 0; it < n_it; ++it) {
-                const int st = it % NST, b = it & 1;
+                const int qs = it % NQS, ds = it % NDS, b = it & 1;
                 if (!wait_bar<kCritSleep>(p_full, it & 1, ctl)) goto mma_teardown;
                 FA_TRACE_EVENT(0, it);
                 tc_fence_after();
                 if constexpr (C::kSDouble) {
-                    // S(it+1) is already in the other buffer; refill dP, then finish tile it
-                    if (it + 1 < n_it) issue_dp((it + 1) % NST);
-                    issue_dv(st, b, it);
-                    issue_dk(st, b, it);
+                    // S(it+1) already sits in the other buffer.  dP(it+1) first (the compute
+                    // warps need it soonest), then dV(it) -- the only reader of P(it), aliased
+                    // in buffer b -- so that S(it+2) can refill buffer b right away.
+                    if (it + 1 < n_it) {
+                        if (!wait_bar<kCritSleep>(do_full((it + 1) % NDS), ((it + 1) / NDS) & 1, ctl))
+                            goto mma_teardown;
+                        tc_fence_after();
+                        issue_dp((it + 1) % NDS);
+                    }
+#pragma unroll
+                    for (int s2 = 0; s2 < NKV; ++s2) step_dv(ds, b, it, s2);
+                    mma_commit(do_empty(ds));
+                    if (it + 2 < n_it) {
+                        if (!wait_bar<kCritSleep>(q_full((it + 2) % NQS), ((it + 2) / NQS) & 1, ctl))
+                            goto mma_teardown;
+                        FA_TRACE_EVENT(11, it);
+                        tc_fence_after();
+                        issue_s((it + 2) % NQS, b);
+                    }
+                    FA_TRACE_EVENT(1, it);
                     if (it > 0) {
                         if (!wait_bar<kCritSleep>(dq_empty, (it - 1) & 1, ctl)) goto mma_teardown;
                         tc_fence_after();
                     }
-                    FA_TRACE_EVENT(1, it);
-                    issue_dq(b);
-                    FA_TRACE_EVENT(10, it);
-                    mma_commit(qdo_empty(st));
-                    mma_commit(ds_empty(b));
-                    // S(it+2) overwrites buffer b: S(it) was read by the compute warps and
-                    // P(it), aliased there, was read by dV(it), issued above
-                    if (it + 2 < n_it) {
-                        const int st2 = (it + 2) % NST;
-                        if (!wait_bar<kCritSleep>(qdo_full(st2), ((it + 2) / NST) & 1, ctl)) goto mma_teardown;
-                        FA_TRACE_EVENT(11, it);
-                        tc_fence_after();
-                        issue_s(st2, b);
+                    // dQ0 dK0 dQ1 dK1 ... dQ3 dK3 dQ4 .. dQ7: alternate accumulators where possible
+#pragma unroll
+                    for (int s2 = 0; s2 < NQ; ++s2) {
+                        step_dq(b, s2);
+                        if (s2 < NKV) step_dk(qs, b, it, s2);
                     }
+                    mma_commit(dq_full);
+                    mma_commit(q_empty(qs));
+                    mma_commit(ds_empty(b));
                     FA_TRACE_EVENT(2, it);
                 } else {
                     // single S buffer (compute(it) has read it): S and dP of it+1 first
                     if (it + 1 < n_it) {
-                        const int st1 = (it + 1) % NST;
-                        if (!wait_bar<kCritSleep>(qdo_full(st1), ((it + 1) / NST) & 1, ctl)) goto mma_teardown;
+                        if (!wait_bar<kCritSleep>(q_full((it + 1) % NQS), ((it + 1) / NQS) & 1, ctl))
+                            goto mma_teardown;
                         tc_fence_after();
-                        issue_s(st1, 0);
-                        issue_dp(st1);
+                        issue_s((it + 1) % NQS, 0);
+                        if (!wait_bar<kCritSleep>(do_full((it + 1) % NDS), ((it + 1) / NDS) & 1, ctl))
+                            goto mma_teardown;
+                        tc_fence_after();
+                        issue_dp((it + 1) % NDS);
                     }
-                    issue_dv(st, b, it);
+#pragma unroll
+                    for (int s2 = 0; s2 < NKV; ++s2) step_dv(ds, b, it, s2);
                     mma_commit(p_free);
-                    issue_dk(st, b, it);
+                    mma_commit(do_empty(ds));
                     if (it > 0) {
                         if (!wait_bar<kCritSleep>(dq_empty, (it - 1) & 1, ctl)) goto mma_teardown;
                         tc_fence_after();
                     }
-                    issue_dq(b);
-                    mma_commit(qdo_empty(st));
+                    // dQ0 dK0 dQ1 dK1 ...
+#pragma unroll
+                    for (int s2 = 0; s2 < NQ; ++s2) {
+                        step_dq(b, s2);
+                        if (s2 < NKV) step_dk(qs, b, it, s2);
+                    }
+                    mma_commit(dq_full);
+                    mma_commit(q_empty(qs));
                     mma_commit(ds_empty(b));
                 }
             }
@@ -457,11 +494,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool prescale = p.prescale != 0;
         constexpr int NCH = C::kHalf / 32;  // 32-column chunks per thread
         for (int it = 0; it < n_it; ++it) {
-            const int st = it % NST, b = it & 1;
+            const int st = it % NQS, b = it & 1;
             const int sb = C::kSDouble ? b : 0;
             const int qt = q_begin + it, q0 = qt * BM;
             const bool masked = bwd_tile_class(T, CAUSAL, BM, qt, kt) == kMasked;
-            if (!warp_wait(qdo_full(st), (it / NST) & 1, ctl)) break;
+            if (!warp_wait(q_full(st), (it / NQS) & 1, ctl)) break;
             if (!warp_wait<kCritSleep>(s_full(sb), C::kSDouble ? ((it >> 1) & 1) : (it & 1), ctl)) break;
             if (warp == 0 && lane == 0) FA_TRACE_EVENT(3, it);
             if (lane == 0) FA_TRACE_EVENT(18 + warp, it);
