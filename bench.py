@@ -350,7 +350,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        heads = [(0, 0), (0, 1)]
+        heads = [(0, h) for h in range(8)]
         sec, fl, threads = time_oracle_heads(w, heads, causal)
         cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"heads (b,h)={heads} of {w.name} at full T, fp64 oracle forward + backward "

@@ -69,3 +69,29 @@ def test_tma_probe_swizzle_and_zero_fill(plib, D, row0, bh):
                 off = (a * box * 128 + r * 128 + ((c ^ (r % 8)) * 16)) // 2
                 want[off:off + 8] = vals
     np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.gpu
+def test_mma_issue_rate_report(plib, capsys):
+    """Issue/complete rate of 128xNx16 bf16 tcgen05.mma chains by operand form.
+
+    Prints the table summarised in profiles/tcgen05_mma_issue_rates.md and
+    checks the dense K-major SS form runs within 30 % of 8192 FLOP/clk at N >= 128."""
+    plib.probe_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong)]
+    names = {1: "SS, A and B K-major", 4: "SS, B MN-major", 5: "SS, A and B MN-major", 6: "TS (A in TMEM), B K-major",
+             7: "TS, B MN-major", 11: "SS K-major, 2 accumulators alternating",
+             9: "SS MN-major, 2 accumulators alternating", 8: "TS B MN-major, 2 accumulators alternating"}
+    rows = []
+    for N in (64, 128, 256):
+        for mode in names:
+            o = (ctypes.c_longlong * 3)()
+            assert plib.probe_mma_rate(N, 256, mode, o) == 0
+            assert plib.probe_mma_rate(N, 256, mode, o) == 0
+            rows.append((N, names[mode], o[1] / 256.0, 128 * N * 16 * 2 / 8192))
+    with capsys.disabled():
+        print("\n  N  form                                       cycles/MMA  ideal")
+        for N, name, c, ideal in rows:
+            print(f"{N:4d}  {name:42s} {c:9.1f} {ideal:6.0f}")
+    for N, name, c, ideal in rows:
+        if name == "SS, A and B K-major" and N >= 128:
+            assert c <= 1.3 * ideal
