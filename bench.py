@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="T sweep (512..8192 at 16384 tokens x 16 heads): one JSON line per case, not the bench line")
     return ap.parse_args()
 
 
@@ -207,8 +209,67 @@ def run_reference(args, w, causal, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def algorithmic_bytes(B, H, T, D, bwd):
+    """Bytes the pass must move at least: each tensor read or written once.
+    Forward: read Q, K, V; write O (bf16) and LSE (fp32).  Backward: read Q,
+    K, V, O, dO, LSE; write dQ, dK, dV; plus the fp32 workspace (D and LSE2
+    written and read, dQ accumulator zeroed, reduced into and read)."""
+    n = B * H * T * D
+    if not bwd:
+        return 2 * 4 * n + 4 * B * H * T
+    return 2 * 8 * n + 4 * B * H * T + 4 * 4 * B * H * T + 4 * 3 * n
+
+
+def run_sweep(args):
+    """T sweep of the forward and the backward (the short-T, memory/latency-bound
+    end against the long-T compute-bound end), 16384 tokens x 16 heads per case."""
+    import torch
+    import online_softmax_05_gb300 as fa
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, src = load_peaks()
+    for D in (64, 128):
+        for causal in (0, 1):
+            for T in (512, 1024, 2048, 4096, 8192):
+                B, H = 16384 // T, 16
+                g = torch.Generator(device="cpu").manual_seed(T + D)
+                q, k, v, do = (torch.randn(B, H, T, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(4))
+                o = torch.empty_like(q)
+                lse = torch.empty(B, H, T, device=dev)
+                dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+                sc = D ** -0.5
+                f = lambda: fa.fa_fwd(q, k, v, o, lse, B, H, T, D, sc, causal, stream)
+                b = lambda: fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, T, D, sc, causal, stream)
+                res = {}
+                for name, fn in (("fwd", f), ("bwd", b)):
+                    for _ in range(max(3, args.warmup)):
+                        assert fn() == 0
+                    torch.cuda.synchronize(dev)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    n = max(10, min(args.steps, 50))
+                    e0.record(stream)
+                    for _ in range(n):
+                        fn()
+                    e1.record(stream)
+                    torch.cuda.synchronize(dev)
+                    res[name] = e0.elapsed_time(e1) / n
+                assert fa.fa_get_device_status(stream) == 0
+                fwd_fl = 4.0 * B * H * T * T * D / (2 if causal else 1)
+                line = {"sweep": "T", "B": B, "H": H, "T": T, "D": D, "causal": bool(causal),
+                        "fwd_ms": res["fwd"], "bwd_ms": res["bwd"],
+                        "fwd_tflops": fwd_fl / res["fwd"] / 1e9, "bwd_tflops": 2.5 * fwd_fl / res["bwd"] / 1e9,
+                        "fwd_gbs": algorithmic_bytes(B, H, T, D, False) / res["fwd"] / 1e6,
+                        "bwd_gbs": algorithmic_bytes(B, H, T, D, True) / res["bwd"] / 1e6,
+                        "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"], "peaks": src}
+                print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
