@@ -64,6 +64,8 @@ def _load():
         lib.oracle_attn_bwd_rows.restype = ctypes.c_int
         lib.oracle_attn_fwd_rows.argtypes = [_D, _D, _D, ctypes.c_long, ctypes.c_long, ctypes.c_double,
                                              ctypes.c_int, ctypes.c_long, _L, _D, _D]
+        lib.oracle_attn_fwd_cross.argtypes = [_D, _D, _D, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                              ctypes.c_double, _D, _D]
         lib.oracle_flash_fwd_tiled.argtypes = [_D, _D, _D, ctypes.c_long, ctypes.c_long, ctypes.c_double,
                                                ctypes.c_int, ctypes.c_long, ctypes.c_long, _D, _D]
         _lib = lib
@@ -174,4 +176,19 @@ def flash_fwd_tiled(q, k, v, scale: float, causal: bool, bq: int, bk: int):
     lse = np.zeros(T)
     _load().oracle_flash_fwd_tiled(_p(q), _p(k), _p(v), T, D, float(scale), int(bool(causal)), int(bq), int(bk),
                                    _p(o), _p(lse))
+    return o, lse
+
+
+def attn_fwd_cross(q, k, v, scale: float):
+    """Tq queries attend to all Tk keys of their head, no mask ([..., Tq, D] / [..., Tk, D]).
+
+    "Lab 06", "Check yourself" item 2 (decoding against a long cache)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Tq, D = q.shape[-2], q.shape[-1]
+    Tk = k.shape[-2]
+    nbh = q.size // (Tq * D) if q.size else 0
+    o = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:-1])
+    if nbh:
+        _load().oracle_attn_fwd_cross(_p(q), _p(k), _p(v), nbh, Tq, Tk, D, float(scale), _p(o), _p(lse))
     return o, lse

@@ -397,3 +397,44 @@ void oracle_flash_fwd_tiled(const double* q, const double* k, const double* v, l
         free(m); free(l); free(acc); free(st);
     }
 }
+
+/*
+ * Naive forward where the Tq queries of a head attend to all Tk keys of the
+ * same head (no mask): the decoding case of "Lab 06", "Check yourself" items
+ * 2 and "Stretch" (one new token against a long cache).  Same definition as
+ * oracle_attn_fwd: O_i = softmax(scale * q_i . K^T) V, LSE_i = m_i + log sum.
+ * q, o: [nbh][Tq][D]; k, v: [nbh][Tk][D]; lse: [nbh][Tq].
+ */
+void oracle_attn_fwd_cross(const double* q, const double* k, const double* v, long nbh, long Tq, long Tk, long D,
+                           double scale, double* o, double* lse) {
+    long rows = nbh * Tq;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)Tk);
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < rows; ++r) {
+            long h = r / Tq, i = r % Tq;
+            const double* qi = q + (h * Tq + i) * D;
+            const double* kh = k + h * Tk * D;
+            const double* vh = v + h * Tk * D;
+            double m = -INFINITY;
+            for (long j = 0; j < Tk; ++j) {
+                s[j] = score(qi, kh + j * D, D, scale);
+                if (s[j] > m) m = s[j];
+            }
+            double sum = 0.0;
+            for (long j = 0; j < Tk; ++j) {
+                s[j] = exp(s[j] - m);
+                sum += s[j];
+            }
+            double* oi = o + (h * Tq + i) * D;
+            for (long d = 0; d < D; ++d) oi[d] = 0.0;
+            for (long j = 0; j < Tk; ++j) {
+                double pj = s[j] / sum;
+                for (long d = 0; d < D; ++d) oi[d] += pj * vh[j * D + d];
+            }
+            lse[h * Tq + i] = m + log(sum);
+        }
+        free(s);
+    }
+}

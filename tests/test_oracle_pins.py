@@ -254,3 +254,38 @@ def test_oracle_on_generated_bf16_inputs_is_finite():
     dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, 0.25, False)
     for a in (o, lse, dq, dk, dv):
         assert np.isfinite(a).all()
+
+
+# --- queries attending to a longer key sequence (decoding) -------------------
+
+def test_cross_equals_square_when_lengths_match():
+    T, D = 31, 8
+    q, k, v = (rng(s).normal(size=(2, T, D)) for s in (50, 51, 52))
+    o1, l1 = oracle.attn_fwd(q, k, v, 0.4, False)
+    o2, l2 = oracle.attn_fwd_cross(q, k, v, 0.4)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("Tq,Tk", [(1, 1), (1, 97), (3, 40), (8, 5)])
+def test_cross_matches_library_softmax(Tq, Tk):
+    D = 6
+    q, k, v = rng(53).normal(size=(2, Tq, D)), rng(54).normal(size=(2, Tk, D)), rng(55).normal(size=(2, Tk, D))
+    o, lse = oracle.attn_fwd_cross(q, k, v, 0.7)
+    for h in range(2):
+        S = 0.7 * (q[h] @ k[h].T)
+        np.testing.assert_allclose(lse[h], scipy.special.logsumexp(S, axis=1), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(o[h], scipy.special.softmax(S, axis=1) @ v[h], rtol=0, atol=1e-12)
+
+
+def test_cross_uniform_scores_and_single_key():
+    # Q = 0: O = mean of all V rows, LSE = log Tk; one key: O = that V row, LSE = its score
+    Tq, Tk, D = 2, 50, 4
+    k, v = rng(56).normal(size=(1, Tk, D)), rng(57).normal(size=(1, Tk, D))
+    o, lse = oracle.attn_fwd_cross(np.zeros((1, Tq, D)), k, v, 1.3)
+    np.testing.assert_allclose(o[0], np.broadcast_to(v[0].mean(axis=0), (Tq, D)), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[0], math.log(Tk), rtol=0, atol=1e-13)
+    q = rng(58).normal(size=(1, Tq, D))
+    o, lse = oracle.attn_fwd_cross(q, k[:, :1], v[:, :1], 1.3)
+    np.testing.assert_array_equal(o[0], np.broadcast_to(v[0, 0], (Tq, D)))
+    np.testing.assert_allclose(lse[0], 1.3 * (q[0] @ k[0, 0]), rtol=0, atol=1e-13)
