@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="split-K decoding: B=8 H=32, 1 query row against 32768 keys, D=128 (HBM-bound)")
     ap.add_argument("--sweep", action="store_true",
                     help="T sweep (512..8192 at 16384 tokens x 16 heads): one JSON line per case, not the bench line")
     return ap.parse_args()
@@ -265,8 +267,49 @@ def run_sweep(args):
                 print(json.dumps(line), flush=True)
 
 
+def run_decode(args, B=8, H=32, Tq=1, Tk=32768, D=128):
+    """fa_decode throughput: one JSON line with GB/s against the measured HBM copy rate."""
+    import torch
+    import online_softmax_05_gb300 as fa
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device="cpu").manual_seed(0)
+    q = torch.randn(B, H, Tq, D, generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn(B, H, Tk, D, generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn(B, H, Tk, D, generator=g).to(torch.bfloat16).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Tq, device=dev)
+    sc = D ** -0.5
+    for _ in range(max(3, args.warmup)):
+        assert fa.fa_decode(q, k, v, o, lse, B, H, Tq, Tk, D, sc, stream) == 0
+    torch.cuda.synchronize(dev)
+    n = max(10, min(args.steps, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fa.fa_decode(q, k, v, o, lse, B, H, Tq, Tk, D, sc, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert fa.fa_get_device_status(stream) == 0
+    ms = e0.elapsed_time(e1) / n
+    nbytes = 2 * (2 * B * H * Tq * D + 2 * B * H * Tk * D) + 4 * B * H * Tq
+    peaks, src = load_peaks()
+    gbs = nbytes / ms / 1e6
+    print(json.dumps({"metric": "split-K decoding GB/s (K/V streamed once)", "value": gbs, "unit": "GB/s",
+                      "ms_per_call": ms, "calls": n, "tflops": 4.0 * B * H * Tq * Tk * D / ms / 1e9,
+                      "config": {"workload": f"decode_b{B}h{H}q{Tq}k{Tk}d{D}", "B": B, "H": H, "Tq": Tq, "Tk": Tk,
+                                 "D": D, "l2": "no flush: K/V %.1f GB > 129 MB L2" % (nbytes / 1e9)},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": gbs / peaks["hbm_gbs"], "peak_kind": f"copy bandwidth, of {src}"},
+                      "dtype": "bf16", "data": "synthetic"}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.decode:
+        run_decode(args)
+        return
     if args.sweep:
         run_sweep(args)
         return

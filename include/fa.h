@@ -47,7 +47,7 @@ extern "C" {
 typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_NULL = -1,            /* a required pointer is NULL */
-    FA_ERR_SHAPE = -2,           /* B, H or T < 1, or a size overflows the index types */
+    FA_ERR_SHAPE = -2,           /* B, H, T (Tq, Tk) out of range, or a size overflows the index types */
     FA_ERR_UNSUPPORTED = -3,     /* D is not 64 or 128 */
     FA_ERR_ALIGN = -4,           /* a base pointer is not 16-byte aligned */
     FA_ERR_CUDA = -5,            /* a CUDA runtime / driver call failed (launch, attribute, tensor map) */
@@ -114,6 +114,24 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                    const float* lse, void* dq, void* dk, void* dv,
                    int B, int H, int T, int D, float scale, int causal, void* stream);
+
+/*
+ * Decoding forward, split over the keys ("Lab 06 - Attention kernels",
+ * "Check yourself" item 2 and "Stretch": a few new query rows against a long
+ * key/value cache).  Each of the Tq query rows of a head attends to ALL Tk
+ * keys of the same head (no mask).  The keys are split into chunks processed
+ * in parallel, each producing a partial (m, l, acc); a second kernel merges
+ * them with the online-softmax rescaling rule.
+ *   q       in : (B, H, Tq, D) bf16, 1 <= Tq <= 8
+ *   k, v    in : (B, H, Tk, D) bf16, Tk >= 1
+ *   o       out: (B, H, Tq, D) bf16
+ *   lse     out: (B, H, Tq) float32, natural-log log-sum-exp of the scaled scores
+ *   scale, stream: as in fa_fwd.  D must be 64 or 128.
+ * Workspace: the partials (B*H*n_chunks*Tq*(D + 2) floats) are taken with
+ * cudaMallocAsync on `stream` and released before returning.
+ */
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int Tq, int Tk, int D, float scale, void* stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* fa_strerror(int status);

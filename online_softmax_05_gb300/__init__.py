@@ -12,7 +12,7 @@ import math
 import os
 import threading
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
+__all__ = ["fa_fwd", "fa_bwd", "fa_decode", "attention_decode", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
            "attention_forward", "attention_backward", "FAError", "library_path", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -51,6 +51,8 @@ def load_library():
         lib.fa_fwd.restype = i
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         lib.fa_bwd.restype = i
+        lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        lib.fa_decode.restype = i
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         lib.fa_bwd_noalloc.restype = i
         lib.fa_strerror.argtypes = [i]
@@ -104,6 +106,30 @@ def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B: int, H: int, T: int, D: int, scal
     """C-ABI ``fa_bwd``; tensors (or raw device pointers) in, status code out."""
     return load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
                                  _ptr(dv), B, H, T, D, float(scale), int(causal), _stream(stream))
+
+
+def fa_decode(q, k, v, o, lse, B: int, H: int, Tq: int, Tk: int, D: int, scale: float, stream=None) -> int:
+    """C-ABI ``fa_decode``: Tq (<= 8) query rows per head against all Tk keys, split over the keys."""
+    return load_library().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, D, float(scale),
+                                    _stream(stream))
+
+
+def attention_decode(q, k, v, scale: float | None = None, out=None, lse=None, stream=None):
+    """O, LSE for q (B, H, Tq, D) against k, v (B, H, Tk, D); all bf16 contiguous CUDA tensors."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    B, H, Tq, D = q.shape
+    Tk = k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Tq), device=q.device, dtype=torch.float32) if lse is None else lse
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_decode(q, k, v, out, lse, B, H, Tq, Tk, D, scale, stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_decode")
+    return out, lse
 
 
 def fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B: int, H: int, T: int, D: int, scale: float, causal: int,

@@ -28,7 +28,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                      f"-I{INCLUDE}", f"-I{CSRC}", "--expt-relaxed-constexpr"]
 
-PRODUCT_UNITS = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu"]
+PRODUCT_UNITS = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu"]
 PROBE_UNITS = ["fa_probe.cu"]
 
 

@@ -81,8 +81,8 @@ const char* fa_strerror(int status) {
     switch (status) {
         case FA_OK: return "ok";
         case FA_ERR_NULL: return "a required pointer is NULL";
-        case FA_ERR_SHAPE: return "B, H and T must be >= 1 and B*H*T must fit in a 32-bit index";
-        case FA_ERR_UNSUPPORTED: return "head dimension D must be 64 or 128";
+        case FA_ERR_SHAPE: return "B, H and T (Tq, Tk) must be >= 1 and B*H*T must fit in a 32-bit index";
+        case FA_ERR_UNSUPPORTED: return "head dimension D must be 64 or 128 (and fa_decode takes at most 8 query rows)";
         case FA_ERR_ALIGN: return "tensor base pointers must be 16-byte aligned";
         case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
         case FA_ERR_NOMEM: return "stream-ordered workspace allocation failed";
@@ -136,6 +136,28 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     if (rc != FA_OK) return rc;
     return fa::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, T, D, scale, causal != 0,
                           static_cast<cudaStream_t>(stream), knobs(), sms);
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Tq, int Tk, int D,
+              float scale, void* stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+    if (B < 1 || H < 1 || Tq < 1 || Tk < 1) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * H > (1 << 30) || static_cast<long long>(B) * H * Tk > INT_MAX) return FA_ERR_SHAPE;
+    if (Tq > 8) return FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return FA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGN;
+    const size_t nq = static_cast<size_t>(B) * H * Tq * D * 2, nk = static_cast<size_t>(B) * H * Tk * D * 2;
+    const size_t nl = static_cast<size_t>(B) * H * Tq * 4;
+    const Range rq = range_of(q, nq), rk = range_of(k, nk), rv = range_of(v, nk), ro = range_of(o, nq),
+                rl = range_of(lse, nl);
+    if (overlap(ro, rq) || overlap(ro, rk) || overlap(ro, rv) || overlap(ro, rl) || overlap(rl, rq) ||
+        overlap(rl, rk) || overlap(rl, rv))
+        return FA_ERR_ARG;
+    int dev = 0, sms = 0;
+    int rc = current_device(&dev, &sms);
+    if (rc != FA_OK) return rc;
+    return fa::launch_decode(q, k, v, o, lse, B, H, Tq, Tk, D, scale, static_cast<cudaStream_t>(stream), sms);
 }
 
 // Same checks as fa_bwd, then the fixed-scratch backward (see include/fa.h:

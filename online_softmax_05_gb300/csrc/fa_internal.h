@@ -21,6 +21,10 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
                void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
                cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
 
+// Split-K decoding forward (fa_decode.cu).
+int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Tq, int Tk,
+                  int D, float scale, cudaStream_t stream, int num_sms);
+
 // Backward with the library's fixed device scratch buffer instead of an
 // allocation; returns -10 if the problem does not fit, without launching.
 size_t bwd_scratch_bytes(int B, int H, int T, int D);

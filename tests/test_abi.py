@@ -96,3 +96,18 @@ def test_debug_knob_validation(lib):
     assert lib.fa_debug_inject(7) == -8
     assert lib.fa_debug_inject(0) == 0
     assert lib.fa_debug_set_wait_timeout_ns(2_000_000_000) == 0
+
+
+def test_argument_errors_decode(lib):
+    base = 0x1000_0000
+    q, k, v, o, lse = base, 2 * base, 3 * base, 4 * base, 5 * base
+    f = lambda **kw: fa.fa_decode(kw.get("q", q), k, v, kw.get("o", o), lse, kw.get("B", 1), 2, kw.get("Tq", 1),
+                                  kw.get("Tk", 100), kw.get("D", 128), kw.get("scale", 0.1), None)
+    assert f(q=None) == -1
+    assert f(Tq=0) == -2
+    assert f(Tk=0) == -2
+    assert f(Tq=9) == -3
+    assert f(D=96) == -3
+    assert f(scale=float("nan")) == -8
+    assert f(q=base + 8) == -4
+    assert f(o=q) == -8
