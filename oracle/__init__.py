@@ -192,3 +192,22 @@ def attn_fwd_cross(q, k, v, scale: float):
     if nbh:
         _load().oracle_attn_fwd_cross(_p(q), _p(k), _p(v), nbh, Tq, Tk, D, float(scale), _p(o), _p(lse))
     return o, lse
+
+
+def attn_fwd_gqa(q, k, v, scale: float, causal: bool):
+    """Grouped-query forward: q [B, Hq, T, D], k/v [B, Hkv, T, D], query head h
+    using key/value head h // (Hq // Hkv) ("Lab 06", "Check yourself" item 7).
+    By definition: repeat each key/value head over its group, then attn_fwd."""
+    g = q.shape[1] // k.shape[1]
+    return attn_fwd(q, np.repeat(_f64(k), g, axis=1), np.repeat(_f64(v), g, axis=1), scale, causal)
+
+
+def attn_bwd_gqa(q, k, v, dout, scale: float, causal: bool):
+    """Gradients of the grouped-query forward: those of the repeated problem,
+    with dK and dV summed over the query heads of each group."""
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    dq, dk_r, dv_r, dvec = attn_bwd(q, np.repeat(_f64(k), g, axis=1), np.repeat(_f64(v), g, axis=1), dout, scale,
+                                    causal)
+    return dq, dk_r.reshape(B, Hkv, g, T, D).sum(axis=2), dv_r.reshape(B, Hkv, g, T, D).sum(axis=2), dvec

@@ -289,3 +289,35 @@ def test_cross_uniform_scores_and_single_key():
     o, lse = oracle.attn_fwd_cross(q, k[:, :1], v[:, :1], 1.3)
     np.testing.assert_array_equal(o[0], np.broadcast_to(v[0, 0], (Tq, D)))
     np.testing.assert_allclose(lse[0], 1.3 * (q[0] @ k[0, 0]), rtol=0, atol=1e-13)
+
+
+# --- grouped-query attention -------------------------------------------------
+
+def test_gqa_group_of_one_is_plain_attention():
+    q, k, v, do = (rng(s).normal(size=(1, 3, 17, 4)) for s in (60, 61, 62, 63))
+    np.testing.assert_array_equal(oracle.attn_fwd_gqa(q, k, v, 0.5, True)[0], oracle.attn_fwd(q, k, v, 0.5, True)[0])
+    for a, b in zip(oracle.attn_bwd_gqa(q, k, v, do, 0.5, True), oracle.attn_bwd(q, k, v, do, 0.5, True)):
+        np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_finite_difference_of_shared_keys(causal):
+    # L = sum over all query heads of dO o O; dK, dV of a shared head collect every head of its group
+    B, Hq, Hkv, T, D = 1, 4, 2, 5, 3
+    q, do = rng(64).normal(size=(B, Hq, T, D)), rng(65).normal(size=(B, Hq, T, D))
+    k, v = rng(66).normal(size=(B, Hkv, T, D)), rng(67).normal(size=(B, Hkv, T, D))
+    scale = 0.9
+    _, dk, dv, _ = oracle.attn_bwd_gqa(q, k, v, do, scale, causal)
+
+    def loss(kk, vv):
+        return float((oracle.attn_fwd_gqa(q, kk, vv, scale, causal)[0] * do).sum())
+
+    h = 1e-6
+    for g, x, is_k in ((dk, k, True), (dv, v, False)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            fd[idx] = ((loss(xp, v) - loss(xm, v)) if is_k else (loss(k, xp) - loss(k, xm))) / (2 * h)
+        assert np.abs(fd - g).max() / max(np.abs(g).max(), 1e-3) < 1e-6
