@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="split-K decoding: B=8 H=32, 1 query row against 32768 keys, D=128 (HBM-bound)")
+    ap.add_argument("--gqa", action="store_true",
+                    help="grouped-query attention: B=2 Hq=16 Hkv=4 T=8192 D=128 causal, fwd and bwd TFLOP/s")
     ap.add_argument("--sweep", action="store_true",
                     help="T sweep (512..8192 at 16384 tokens x 16 heads): one JSON line per case, not the bench line")
     return ap.parse_args()
@@ -305,8 +307,50 @@ def run_decode(args, B=8, H=32, Tq=1, Tk=32768, D=128):
                       "dtype": "bf16", "data": "synthetic"}), flush=True)
 
 
+def run_gqa(args, B=2, Hq=16, Hkv=4, T=8192, D=128, causal=1):
+    """fa_fwd_gqa / fa_bwd_gqa throughput on the long-context causal shape with 4 query heads per K/V head."""
+    import torch
+    import online_softmax_05_gb300 as fa
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device="cpu").manual_seed(0)
+    q, do = (torch.randn(B, Hq, T, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(2))
+    k, v = (torch.randn(B, Hkv, T, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(2))
+    o, dq = torch.empty_like(q), torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty(B, Hq, T, device=dev)
+    sc = D ** -0.5
+    f = lambda: fa.fa_fwd_gqa(q, k, v, o, lse, B, Hq, Hkv, T, D, sc, causal, stream)
+    b = lambda: fa.fa_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, T, D, sc, causal, stream)
+    res = {}
+    for name, fn in (("fwd", f), ("bwd", b)):
+        for _ in range(max(3, args.warmup)):
+            assert fn() == 0
+        torch.cuda.synchronize(dev)
+        n = max(10, min(args.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = e0.elapsed_time(e1) / n
+    assert fa.fa_get_device_status(stream) == 0
+    fwd_fl = 4.0 * B * Hq * T * T * D / (2 if causal else 1)
+    peaks, src = load_peaks()
+    print(json.dumps({"metric": "grouped-query attention TFLOP/s", "value": 3.5 * fwd_fl / (res["fwd"] + res["bwd"]) / 1e9,
+                      "unit": "TFLOP/s", "fwd_ms": res["fwd"], "bwd_ms": res["bwd"],
+                      "fwd_tflops": fwd_fl / res["fwd"] / 1e9, "bwd_tflops": 2.5 * fwd_fl / res["bwd"] / 1e9,
+                      "config": {"workload": f"gqa_b{B}hq{Hq}hkv{Hkv}t{T}d{D}", "causal": bool(causal)},
+                      "peak": peaks["bf16_tflops"], "peaks": src, "dtype": "bf16", "data": "synthetic"}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.gqa:
+        run_gqa(args)
+        return
     if args.decode:
         run_decode(args)
         return

@@ -116,6 +116,25 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    int B, int H, int T, int D, float scale, int causal, void* stream);
 
 /*
+ * Grouped-query attention ("Lab 06 - Attention kernels", "Check yourself"
+ * item 7): Hq query heads share Hkv key/value heads, Hq % Hkv == 0, query
+ * head h using key/value head h / (Hq / Hkv).  Same computation, layout,
+ * asynchrony and errors as fa_fwd / fa_bwd with
+ *   q, o, dO, dq : (B, Hq, T, D) bf16;  lse : (B, Hq, T) float32
+ *   k, v, dk, dv : (B, Hkv, T, D) bf16
+ * dk and dv sum the contributions of every query head of the group.  The
+ * forward pairs two query heads of one group on the same rows in a CTA, so
+ * each K/V tile loaded into shared memory serves both; the backward walks the
+ * query tiles of the whole group per key tile.  Hkv == Hq is plain attention.
+ * FA_ERR_SHAPE if Hq or Hkv < 1 or Hq % Hkv != 0.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int Hq, int Hkv, int T, int D, float scale, int causal, void* stream);
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+               const float* lse, void* dq, void* dk, void* dv,
+               int B, int Hq, int Hkv, int T, int D, float scale, int causal, void* stream);
+
+/*
  * Decoding forward, split over the keys ("Lab 06 - Attention kernels",
  * "Check yourself" item 2 and "Stretch": a few new query rows against a long
  * key/value cache).  Each of the Tq query rows of a head attends to ALL Tk

@@ -12,7 +12,7 @@ import math
 import os
 import threading
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_decode", "attention_decode", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "attention_decode", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
            "attention_forward", "attention_backward", "FAError", "library_path", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -51,6 +51,10 @@ def load_library():
         lib.fa_fwd.restype = i
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         lib.fa_bwd.restype = i
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_gqa.restype = i
+        lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_bwd_gqa.restype = i
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.fa_decode.restype = i
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -106,6 +110,20 @@ def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B: int, H: int, T: int, D: int, scal
     """C-ABI ``fa_bwd``; tensors (or raw device pointers) in, status code out."""
     return load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
                                  _ptr(dv), B, H, T, D, float(scale), int(causal), _stream(stream))
+
+
+def fa_fwd_gqa(q, k, v, o, lse, B: int, Hq: int, Hkv: int, T: int, D: int, scale: float, causal: int,
+               stream=None) -> int:
+    """C-ABI ``fa_fwd_gqa``: Hq query heads over Hkv shared key/value heads."""
+    return load_library().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, D, float(scale),
+                                     int(causal), _stream(stream))
+
+
+def fa_bwd_gqa(q, k, v, o, dO, lse, dq, dk, dv, B: int, Hq: int, Hkv: int, T: int, D: int, scale: float,
+               causal: int, stream=None) -> int:
+    """C-ABI ``fa_bwd_gqa``; dk, dv sum over each group of query heads."""
+    return load_library().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), B, Hq, Hkv, T, D, float(scale), int(causal), _stream(stream))
 
 
 def fa_decode(q, k, v, o, lse, B: int, H: int, Tq: int, Tk: int, D: int, scale: float, stream=None) -> int:

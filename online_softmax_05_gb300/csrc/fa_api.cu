@@ -94,14 +94,21 @@ const char* fa_strerror(int status) {
     }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int D, float scale,
-           int causal, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared checks and dispatch of the forward; Hq query heads over Hkv K/V heads.
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int T, int D,
+             float scale, int causal, void* stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
-    int rc = check_shape(B, H, T, D, scale, causal);
+    if (Hkv < 1 || Hq < 1 || Hq % Hkv != 0) return FA_ERR_SHAPE;
+    int rc = check_shape(B, Hq, T, D, scale, causal);
     if (rc != FA_OK) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGN;
-    const size_t n = static_cast<size_t>(B) * H * T * D * 2, nl = static_cast<size_t>(B) * H * T * 4;
-    const Range rq = range_of(q, n), rk = range_of(k, n), rv = range_of(v, n), ro = range_of(o, n),
+    const size_t nq = static_cast<size_t>(B) * Hq * T * D * 2, nk = static_cast<size_t>(B) * Hkv * T * D * 2;
+    const size_t nl = static_cast<size_t>(B) * Hq * T * 4;
+    const Range rq = range_of(q, nq), rk = range_of(k, nk), rv = range_of(v, nk), ro = range_of(o, nq),
                 rl = range_of(lse, nl);
     if (overlap(ro, rq) || overlap(ro, rk) || overlap(ro, rv) || overlap(ro, rl) || overlap(rl, rq) ||
         overlap(rl, rk) || overlap(rl, rv))
@@ -109,22 +116,25 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     int dev = 0, sms = 0;
     rc = current_device(&dev, &sms);
     if (rc != FA_OK) return rc;
-    return fa::launch_fwd(q, k, v, o, lse, B, H, T, D, scale, causal != 0, static_cast<cudaStream_t>(stream),
+    return fa::launch_fwd(q, k, v, o, lse, B, Hq, Hkv, T, D, scale, causal != 0, static_cast<cudaStream_t>(stream),
                           knobs(), sms);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
-           void* dk, void* dv, int B, int H, int T, int D, float scale, int causal, void* stream) {
+// Shared checks and dispatch of the backward.
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+             void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, int causal, void* stream) {
     if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
-    int rc = check_shape(B, H, T, D, scale, causal);
+    if (Hkv < 1 || Hq < 1 || Hq % Hkv != 0) return FA_ERR_SHAPE;
+    int rc = check_shape(B, Hq, T, D, scale, causal);
     if (rc != FA_OK) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return FA_ERR_ALIGN;
-    const size_t n = static_cast<size_t>(B) * H * T * D * 2, nl = static_cast<size_t>(B) * H * T * 4;
-    const Range ins[6] = {range_of(q, n), range_of(k, n), range_of(v, n), range_of(o, n), range_of(dO, n),
+    const size_t nq = static_cast<size_t>(B) * Hq * T * D * 2, nk = static_cast<size_t>(B) * Hkv * T * D * 2;
+    const size_t nl = static_cast<size_t>(B) * Hq * T * 4;
+    const Range ins[6] = {range_of(q, nq), range_of(k, nk), range_of(v, nk), range_of(o, nq), range_of(dO, nq),
                           range_of(lse, nl)};
-    const Range outs[3] = {range_of(dq, n), range_of(dk, n), range_of(dv, n)};
+    const Range outs[3] = {range_of(dq, nq), range_of(dk, nk), range_of(dv, nk)};
     for (int a = 0; a < 3; ++a) {
         for (int b = 0; b < 6; ++b)
             if (overlap(outs[a], ins[b])) return FA_ERR_ARG;
@@ -134,8 +144,32 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     int dev = 0, sms = 0;
     rc = current_device(&dev, &sms);
     if (rc != FA_OK) return rc;
-    return fa::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, T, D, scale, causal != 0,
+    return fa::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, T, D, scale, causal != 0,
                           static_cast<cudaStream_t>(stream), knobs(), sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int D, float scale,
+           int causal, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, H, T, D, scale, causal, stream);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+           void* dk, void* dv, int B, int H, int T, int D, float scale, int causal, void* stream) {
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, T, D, scale, causal, stream);
+}
+
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int T,
+               int D, float scale, int causal, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, T, D, scale, causal, stream);
+}
+
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+               void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, int causal, void* stream) {
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, T, D, scale, causal, stream);
 }
 
 int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Tq, int Tk, int D,

@@ -112,7 +112,8 @@ struct BwdParams {
     float* dqacc;        // [BH][T][D]
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
-    int T, T_pad, BH, n_kt;
+    int T, T_pad, BH, n_kt;  // BH = batch * key/value heads (one CTA row per K/V head)
+    int Hq, Hkv, group;       // query heads, key/value heads, Hq / Hkv
     float scale;
     float sl2, sl2_eff;
     int prescale;
@@ -260,10 +261,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T;
     // head-major order: the key tiles of one head run together (their Q, dO
-    // and dQ accumulator stay in L2); within a head, heavy key tiles first
-    const int bh = blockIdx.x / p.n_kt, kt = blockIdx.x % p.n_kt;
+    // and dQ accumulator stay in L2); within a head, heavy key tiles first.
+    // With grouped heads the CTA walks the query tiles of every query head that
+    // shares this K/V head, so dK and dV sum over the group in TMEM.
+    const int bh = blockIdx.x / p.n_kt, kt = blockIdx.x % p.n_kt;  // bh: batch * Hkv + K/V head
     const int q_begin = bwd_q_begin(T, CAUSAL, kt, BM), q_end = bwd_q_end(T, BM);
-    const int n_it = q_end - q_begin;
+    const int n_q = q_end - q_begin;
+    const int n_it = n_q * p.group;
+    const int bhq0 = (bh / p.Hkv) * p.Hq + (bh % p.Hkv) * p.group;  // first query head of the group
+    auto q_tile_of = [&](int it) { return q_begin + it % n_q; };
+    auto q_head_of = [&](int it) { return bhq0 + it / n_q; };
 
     if (tid == 0) {
         mbar_init(kv_full, 1);
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d_hint(sV + a * 128 * 128, &tm_v, kv_full, 64 * a, kt * kBN, bh, pol_kv);
             }
             for (int it = 0; it < n_it; ++it) {
-                const int qt = q_begin + it;
+                const int qt = q_tile_of(it), bhq = q_head_of(it);
                 {   // Q tile with its -LSE2 and -D vectors
                     const int st = it % NQS;
                     if (!wait_bar(q_empty(st), ((it / NQS) & 1) ^ 1, ctl)) break;
@@ -318,8 +325,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mbar_arrive_expect_tx(fb, C::kQBytes + 2 * BM * 4);
                     ++q_armed;
                     for (int a = 0; a < C::kAtomsD; ++a)
-                        tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qt * BM, bh, pol_q);
-                    const size_t voff = static_cast<size_t>(bh) * p.T_pad + static_cast<size_t>(qt) * BM;
+                        tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qt * BM, bhq, pol_q);
+                    const size_t voff = static_cast<size_t>(bhq) * p.T_pad + static_cast<size_t>(qt) * BM;
                     bulk_load_1d(sLse(st), p.lse2 + voff, BM * 4, fb);
                     bulk_load_1d(sDv(st), p.dvec + voff, BM * 4, fb);
                 }
@@ -330,7 +337,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mbar_arrive_expect_tx(fb, C::kQBytes);
                     ++do_armed;
                     for (int a = 0; a < C::kAtomsD; ++a)
-                        tma_load_3d_hint(sdO(st) + a * BM * 128, &tm_do, fb, 64 * a, qt * BM, bh, pol_q);
+                        tma_load_3d_hint(sdO(st) + a * BM * 128, &tm_do, fb, 64 * a, qt * BM, bhq, pol_q);
                 }
             }
             // drain: copies still in flight must land before the CTA exits
@@ -496,7 +503,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int it = 0; it < n_it; ++it) {
             const int st = it % NQS, b = it & 1;
             const int sb = C::kSDouble ? b : 0;
-            const int qt = q_begin + it, q0 = qt * BM;
+            const int qt = q_tile_of(it), q0 = qt * BM;
             const bool masked = bwd_tile_class(T, CAUSAL, BM, qt, kt) == kMasked;
             if (!warp_wait(q_full(st), (it / NQS) & 1, ctl)) break;
             if (!warp_wait<kCritSleep>(s_full(sb), C::kSDouble ? ((it >> 1) & 1) : (it & 1), ctl)) break;
@@ -600,7 +607,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int r = 32 * wq + lane;  // TMEM lane of this thread
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int q0 = (q_begin + it) * BM;
+            const int q0 = q_tile_of(it) * BM, bhq = q_head_of(it);
             if (!warp_wait(dq_full, it & 1, ctl)) {
                 ok = false;
                 break;
@@ -619,7 +626,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(dq_empty);
             if constexpr (C::kDqT) {
                 // lane = d; columns = queries q0 .. q0+63
-                float* base = p.dqacc + (static_cast<size_t>(bh) * T + q0) * D + r;
+                float* base = p.dqacc + (static_cast<size_t>(bhq) * T + q0) * D + r;
                 if (q0 + 64 <= T) {
 #pragma unroll
                     for (int e = 0; e < 64; ++e) atomicAdd(base + static_cast<size_t>(e) * D, __uint_as_float(v[e]));
@@ -631,7 +638,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             } else {
                 // lane = query row q0 + r; columns = d
                 if (q0 + r < T) {
-                    float* base = p.dqacc + (static_cast<size_t>(bh) * T + q0 + r) * D;
+                    float* base = p.dqacc + (static_cast<size_t>(bhq) * T + q0 + r) * D;
 #pragma unroll
                     for (int e = 0; e < 64; e += 4)
                         red_add_v4_f32(base + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
@@ -697,9 +704,10 @@ int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
 }  // namespace
 
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-               void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
+               void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, bool causal,
                cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
-    const int BH = B * H;
+    const int BH = B * Hq;        // query heads: D, LSE2, dQ accumulator, Q/dO tensor maps
+    const int BHkv = B * Hkv;     // key/value heads: K/V tensor maps, grid rows
     const int T_pad = cdiv(T, 128) * 128;
     const size_t n_vec = static_cast<size_t>(BH) * T_pad;
     const size_t n_acc = static_cast<size_t>(BH) * T * D;
@@ -716,8 +724,8 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
     int rc = 0;
     CUtensorMap tq, tk, tv, tdo;
     const int bm = bwd_bm(D);
-    if (!make_tmap_bhtd(&tq, q, BH, T, D, bm) || !make_tmap_bhtd(&tk, k, BH, T, D, 128) ||
-        !make_tmap_bhtd(&tv, v, BH, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, bm)) {
+    if (!make_tmap_bhtd(&tq, q, BH, T, D, bm) || !make_tmap_bhtd(&tk, k, BHkv, T, D, 128) ||
+        !make_tmap_bhtd(&tv, v, BHkv, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, bm)) {
         rc = -5;
     } else {
         const long long rows = static_cast<long long>(BH) * T_pad;
@@ -742,7 +750,10 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
             p.dv = static_cast<__nv_bfloat16*>(dv);
             p.T = T;
             p.T_pad = T_pad;
-            p.BH = BH;
+            p.BH = BHkv;
+            p.Hq = Hq;
+            p.Hkv = Hkv;
+            p.group = Hq / Hkv;
             p.n_kt = cdiv(T, kBN);
             p.scale = scale;
             p.sl2 = scale * kLog2e;
@@ -845,6 +856,8 @@ int launch_bwd_noalloc(const void* q, const void* k, const void* v, const void* 
     p.T = T;
     p.T_pad = T_pad;
     p.BH = BH;
+    p.Hq = p.Hkv = H;
+    p.group = 1;
     p.n_kt = cdiv(T, kBN);
     p.scale = scale;
     p.sl2 = scale * kLog2e;

@@ -88,6 +88,9 @@ struct FwdCfg {
 struct FwdParams {
     float* lse;
     int T, BH, n_pairs, n_items;
+    int Hq, Hkv, group;   // query heads, key/value heads, Hq / Hkv
+    int head_pairs;       // 1: the two query tiles of an item are two heads of one group at the same rows
+    int n_tiles;          // query tiles per head
     float sl2_eff;  // multiplier applied inside exp2: scale*log2e, or 1 when prescaled
     float sl2;      // scale * log2(e)
     int prescale;   // 1 when scale <= 0: scores are multiplied by sl2 before the max
@@ -132,8 +135,41 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) 
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// A work item: two 128-row query tiles that share every K/V tile they read.
+// Without grouped heads (or with an odd group) they are consecutive tiles of
+// one head; with an even group of query heads per K/V head they are the same
+// rows of two heads of one group ("Lab 06", "Check yourself" item 7: a K/V
+// tile loaded once serves several query heads).
+struct FwdItem {
+    int tile[2];  // query tile index of each half
+    int bh[2];    // batch * Hq + query head of each half
+    int bh_kv;    // batch * Hkv + key/value head
+    bool valid1;  // the second half has rows < T
+};
+__device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
+    FwdItem it;
+    if (p.head_pairs) {
+        const int per_t = p.BH / 2;  // head pairs over all batches
+        const int t = p.n_tiles - 1 - w / per_t, rem = w % per_t;
+        const int hp = rem % (p.Hq / 2), b = rem / (p.Hq / 2);
+        it.tile[0] = it.tile[1] = t;
+        it.bh[0] = b * p.Hq + 2 * hp;
+        it.bh[1] = it.bh[0] + 1;
+        it.bh_kv = b * p.Hkv + (2 * hp) / p.group;
+        it.valid1 = true;
+    } else {
+        const int pair = p.n_pairs - 1 - w / p.BH, bh = w % p.BH;
+        it.tile[0] = 2 * pair;
+        it.tile[1] = 2 * pair + 1;
+        it.bh[0] = it.bh[1] = bh;
+        it.bh_kv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
+        it.valid1 = it.tile[1] * kFwdBM < p.T;
+    }
+    return it;
+}
+
 // Item k of this CTA in snake order over items sorted heaviest first
-// (causal: later query pairs see more key tiles).
+// (causal: later query tiles see more key tiles).
 __device__ __forceinline__ int item_of(int k, int n_items) {
     int G = gridDim.x;
     int w = k * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
@@ -205,12 +241,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int k = 0;; ++k) {
                 int w = item_of(k, p.n_items);
                 if (w < 0) break;
-                const int pair = p.n_pairs - 1 - w / p.BH, bh = w % p.BH;
-                const int t0 = 2 * pair, t1 = t0 + 1;
-                const bool valid1 = t1 * kFwdBM < T;
-                const int n0 = fwd_num_kv_tiles(T, CAUSAL, t0);
-                const int n1 = valid1 ? fwd_num_kv_tiles(T, CAUSAL, t1) : 0;
+                const FwdItem item = fwd_item(w, p);
+                const bool valid1 = item.valid1;
+                const int n0 = fwd_num_kv_tiles(T, CAUSAL, item.tile[0]);
+                const int n1 = valid1 ? fwd_num_kv_tiles(T, CAUSAL, item.tile[1]) : 0;
                 const int nmax = n0 > n1 ? n0 : n1;
+                const int bh = item.bh_kv;
                 for (int t = 0; t < 2; ++t) {
                     if (t == 1 && !valid1) continue;
                     if (!wait_bar(q_empty(t), (q_cnt[t] & 1) ^ 1, ctl)) goto producer_done;
@@ -218,8 +254,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     mbar_arrive_expect_tx(q_full(t), C::kTileBytes);
                     ++q_armed[t];
                     for (int a = 0; a < C::kAtoms; ++a)
-                        tma_load_3d_hint(sQ[t] + a * C::kAtomBytes, &tm_q, q_full(t), 64 * a, (t0 + t) * kFwdBM, bh,
-                                         pol_q);
+                        tma_load_3d_hint(sQ[t] + a * C::kAtomBytes, &tm_q, q_full(t), 64 * a,
+                                         item.tile[t] * kFwdBM, item.bh[t], pol_q);
                 }
                 for (int j = 0; j < nmax; ++j) {
                     for (int kind = 0; kind < 2; ++kind) {
@@ -278,11 +314,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int k = 0;; ++k) {
                 int w = item_of(k, p.n_items);
                 if (w < 0) break;
-                const int pair = p.n_pairs - 1 - w / p.BH;
-                const int t0 = 2 * pair, t1 = t0 + 1;
-                const bool valid1 = t1 * kFwdBM < T;
-                const int n0 = fwd_num_kv_tiles(T, CAUSAL, t0);
-                const int n1 = valid1 ? fwd_num_kv_tiles(T, CAUSAL, t1) : 0;
+                const FwdItem item = fwd_item(w, p);
+                const bool valid1 = item.valid1;
+                const int n0 = fwd_num_kv_tiles(T, CAUSAL, item.tile[0]);
+                const int n1 = valid1 ? fwd_num_kv_tiles(T, CAUSAL, item.tile[1]) : 0;
                 const int nmax = n0 > n1 ? n0 : n1;
                 if (!wait_bar(q_full(0), q_cnt[0] & 1, ctl)) goto mma_done_label;
                 ++q_cnt[0];
@@ -361,8 +396,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int k = 0;; ++k) {
             int w = item_of(k, p.n_items);
             if (w < 0) break;
-            const int pair = p.n_pairs - 1 - w / p.BH, bh = w % p.BH;
-            const int tile = 2 * pair + t;
+            const FwdItem item = fwd_item(w, p);
+            const int tile = item.tile[t], bh = item.bh[t];
             if (tile * kFwdBM >= T) continue;  // tile 1 of the last pair may be empty
             const int row = tile * kFwdBM + r_local;
             const int n = fwd_num_kv_tiles(T, CAUSAL, tile);
@@ -534,19 +569,24 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 
 }  // namespace
 
-int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int D,
-               float scale, bool causal, cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
-    const int BH = B * H;
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int T,
+               int D, float scale, bool causal, cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
+    const int BH = B * Hq, BHkv = B * Hkv;
     CUtensorMap tq, tk, tv, to;
-    if (!make_tmap_bhtd(&tq, q, BH, T, D, 128) || !make_tmap_bhtd(&tk, k, BH, T, D, 128) ||
-        !make_tmap_bhtd(&tv, v, BH, T, D, 128) || !make_tmap_bhtd(&to, o, BH, T, D, 128))
+    if (!make_tmap_bhtd(&tq, q, BH, T, D, 128) || !make_tmap_bhtd(&tk, k, BHkv, T, D, 128) ||
+        !make_tmap_bhtd(&tv, v, BHkv, T, D, 128) || !make_tmap_bhtd(&to, o, BH, T, D, 128))
         return -5;
     FwdParams p;
     p.lse = lse;
     p.T = T;
     p.BH = BH;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.n_tiles = cdiv(T, kFwdBM);
     p.n_pairs = cdiv(T, 2 * kFwdBM);
-    p.n_items = p.n_pairs * BH;
+    p.head_pairs = (p.group % 2 == 0) ? 1 : 0;
+    p.n_items = p.head_pairs ? p.n_tiles * (BH / 2) : p.n_pairs * BH;
     p.sl2 = scale * kLog2e;
     p.prescale = (p.sl2 > 0.f) ? 0 : 1;
     p.sl2_eff = p.prescale ? 1.f : p.sl2;

@@ -15,10 +15,11 @@ struct DebugKnobs {
 constexpr int kStatusTimeout = -7;
 
 // Launchers: arguments already validated by the C-ABI layer.
-int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int D,
-               float scale, bool causal, cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
+// Hq query heads share Hkv key/value heads (Hq % Hkv == 0; Hkv == Hq is plain attention).
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int T,
+               int D, float scale, bool causal, cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-               void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
+               void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, bool causal,
                cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
 
 // Split-K decoding forward (fa_decode.cu).

@@ -111,3 +111,12 @@ def test_argument_errors_decode(lib):
     assert f(scale=float("nan")) == -8
     assert f(q=base + 8) == -4
     assert f(o=q) == -8
+
+
+def test_argument_errors_gqa(lib):
+    base = 0x1000_0000
+    p = [base * (i + 1) for i in range(9)]
+    assert fa.fa_fwd_gqa(p[0], p[1], p[2], p[3], p[4], 1, 6, 4, 64, 128, 0.1, 0, None) == -2   # 6 % 4 != 0
+    assert fa.fa_fwd_gqa(p[0], p[1], p[2], p[3], p[4], 1, 4, 0, 64, 128, 0.1, 0, None) == -2
+    assert fa.fa_bwd_gqa(*p, 1, 4, 8, 64, 128, 0.1, 0, None) == -2                               # Hkv > Hq
+    assert fa.fa_bwd_gqa(*p[:8], None, 1, 4, 2, 64, 128, 0.1, 0, None) == -1
