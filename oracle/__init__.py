@@ -211,3 +211,25 @@ def attn_bwd_gqa(q, k, v, dout, scale: float, causal: bool):
     dq, dk_r, dv_r, dvec = attn_bwd(q, np.repeat(_f64(k), g, axis=1), np.repeat(_f64(v), g, axis=1), dout, scale,
                                     causal)
     return dq, dk_r.reshape(B, Hkv, g, T, D).sum(axis=2), dv_r.reshape(B, Hkv, g, T, D).sum(axis=2), dvec
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, scale: float, causal: bool):
+    """Packed variable-length forward: q/k/v [total, H, D]; sequence s is rows
+    cu_seqlens[s]:cu_seqlens[s+1] and attends only to itself, causal mask
+    aligned to its own first token ("Triton FlashAttention-2 forward",
+    "Exercises", the cu_seqlens packing).  By definition: attn_fwd on each
+    sequence's slice.  Returns (O [total, H, D], LSE [H, total])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    total, H, D = q.shape
+    cu = [int(c) for c in np.asarray(cu_seqlens).ravel()]
+    o = np.zeros((total, H, D))
+    lse = np.zeros((H, total))
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        if b <= a:
+            continue
+        os_, ls_ = attn_fwd(q[a:b].transpose(1, 0, 2), k[a:b].transpose(1, 0, 2), v[a:b].transpose(1, 0, 2),
+                            scale, causal)
+        o[a:b] = os_.transpose(1, 0, 2)
+        lse[:, a:b] = ls_
+    return o, lse

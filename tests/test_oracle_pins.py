@@ -321,3 +321,36 @@ def test_gqa_finite_difference_of_shared_keys(causal):
             xm[idx] -= h
             fd[idx] = ((loss(xp, v) - loss(xm, v)) if is_k else (loss(k, xp) - loss(k, xm))) / (2 * h)
         assert np.abs(fd - g).max() / max(np.abs(g).max(), 1e-3) < 1e-6
+
+
+# --- packed variable-length sequences ("Triton FlashAttention-2 forward", "Exercises") ---
+
+def test_varlen_single_sequence_is_plain_attention():
+    q, k, v = (rng(40 + i).normal(size=(37, 3, 8)) for i in range(3))
+    o, lse = oracle.attn_fwd_varlen(q, k, v, [0, 37], 0.6, True)
+    o2, l2 = oracle.attn_fwd(q.transpose(1, 0, 2), k.transpose(1, 0, 2), v.transpose(1, 0, 2), 0.6, True)
+    np.testing.assert_array_equal(o, o2.transpose(1, 0, 2))
+    np.testing.assert_array_equal(lse, l2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_matches_block_diagonal_softmax(causal):
+    # brute force over the whole packed batch: one (total x total) score matrix
+    # per head, keys of other sequences (and, causally, later keys of the same
+    # sequence, counted from that sequence's start) set to -inf, library softmax
+    cu = [0, 5, 5, 17, 18, 40]
+    total, H, D, scale = cu[-1], 2, 6, 0.45
+    q, k, v = (rng(50 + i).normal(size=(total, H, D)) * 2.0 for i in range(3))
+    o, lse = oracle.attn_fwd_varlen(q, k, v, np.array(cu, dtype=np.int32), scale, causal)
+    seq = np.zeros(total, dtype=int)
+    pos = np.zeros(total, dtype=int)
+    for s in range(len(cu) - 1):
+        seq[cu[s]:cu[s + 1]] = s
+        pos[cu[s]:cu[s + 1]] = np.arange(cu[s + 1] - cu[s])
+    allowed = seq[:, None] == seq[None, :]
+    if causal:
+        allowed &= pos[None, :] <= pos[:, None]
+    for h in range(H):
+        S = np.where(allowed, scale * q[:, h] @ k[:, h].T, -np.inf)
+        np.testing.assert_allclose(o[:, h], scipy.special.softmax(S, axis=1) @ v[:, h], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[h], scipy.special.logsumexp(S, axis=1), rtol=1e-12, atol=1e-12)
