@@ -62,6 +62,9 @@ def parse_args():
                     help="split-K decoding: B=8 H=32, 1 query row against 32768 keys, D=128 (HBM-bound)")
     ap.add_argument("--gqa", action="store_true",
                     help="grouped-query attention: B=2 Hq=16 Hkv=4 T=8192 D=128 causal, fwd and bwd TFLOP/s")
+    ap.add_argument("--varlen", action="store_true",
+                    help="packed variable-length forward: 48 causal requests of 128..8192 tokens, H=16, D=128, "
+                         "against the same batch padded to the longest request")
     ap.add_argument("--sweep", action="store_true",
                     help="T sweep (512..8192 at 16384 tokens x 16 heads): one JSON line per case, not the bench line")
     return ap.parse_args()
@@ -346,8 +349,61 @@ def run_gqa(args, B=2, Hq=16, Hkv=4, T=8192, D=128, causal=1):
                       "peak": peaks["bf16_tflops"], "peaks": src, "dtype": "bf16", "data": "synthetic"}), flush=True)
 
 
+def run_varlen(args, n_seq=48, H=16, D=128, causal=1):
+    """fa_fwd_varlen throughput on a seeded serving mix, beside fa_fwd on the padded batch."""
+    import numpy as np
+    import torch
+    import online_softmax_05_gb300 as fa
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    lengths = np.random.default_rng(0).integers(128, 8193, size=n_seq)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    total, Tmax = int(cu[-1]), int(lengths.max())
+    g = torch.Generator(device="cpu").manual_seed(0)
+    q, k, v = (torch.randn(total, H, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(3))
+    o = torch.empty_like(q)
+    lse = torch.empty(H, total, device=dev)
+    cud = torch.from_numpy(cu).to(dev)
+    qp, kp, vp = (torch.zeros(n_seq, H, Tmax, D, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    op = torch.empty_like(qp)
+    lp = torch.empty(n_seq, H, Tmax, device=dev)
+    sc = D ** -0.5
+    f = lambda: fa.fa_fwd_varlen(q, k, v, o, lse, cud, n_seq, Tmax, total, H, D, sc, causal, stream)
+    fp = lambda: fa.fa_fwd(qp, kp, vp, op, lp, n_seq, H, Tmax, D, sc, causal, stream)
+    res = {}
+    for name, fn in (("varlen", f), ("padded", fp)):
+        for _ in range(max(3, args.warmup)):
+            assert fn() == 0
+        torch.cuda.synchronize(dev)
+        n = max(10, min(args.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = e0.elapsed_time(e1) / n
+    assert fa.fa_get_device_status(stream) == 0
+    L = lengths.astype(np.float64)
+    useful = float(np.sum(4.0 * H * L * L * D / (2 if causal else 1)))
+    peaks, src = load_peaks()
+    tf = useful / res["varlen"] / 1e9
+    print(json.dumps({"metric": "packed variable-length forward TFLOP/s (useful work)", "value": tf,
+                      "unit": "TFLOP/s", "ms_per_call": res["varlen"], "padded_ms_per_call": res["padded"],
+                      "padded_useful_tflops": useful / res["padded"] / 1e9, "speedup_vs_padded": res["padded"] / res["varlen"],
+                      "frac_of_burst": tf / peaks["bf16_tflops"],
+                      "config": {"workload": f"varlen_n{n_seq}h{H}d{D}_len128to8192", "total_tokens": total,
+                                 "max_seqlen": Tmax, "causal": bool(causal), "lengths": "uniform 128..8192, seed 0",
+                                 "l2": "no flush: Q/K/V %.1f GB > 129 MB L2" % (3 * total * H * D * 2 / 1e9)},
+                      "peak": peaks["bf16_tflops"], "peaks": src, "dtype": "bf16", "data": "synthetic"}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.varlen:
+        run_varlen(args)
+        return
     if args.gqa:
         run_gqa(args)
         return

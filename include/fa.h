@@ -55,7 +55,8 @@ typedef enum fa_status {
     FA_ERR_DEVICE_TIMEOUT = -7,  /* a kernel's bounded wait ran out (pipeline stall); outputs invalid */
     FA_ERR_ARG = -8,             /* causal not 0/1, or scale not finite */
     FA_ERR_ARCH = -9,            /* current device is not compute capability 10.3 (sm_103a) */
-    FA_ERR_SCRATCH = -10         /* fa_bwd_noalloc: problem needs more than its fixed scratch buffer */
+    FA_ERR_SCRATCH = -10,        /* fa_bwd_noalloc: problem needs more than its fixed scratch buffer */
+    FA_ERR_SEQLEN = -11          /* recorded by a kernel: a cu_seqlens length is negative or above max_seqlen */
 } fa_status;
 
 /*
@@ -135,6 +136,27 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                int B, int Hq, int Hkv, int T, int D, float scale, int causal, void* stream);
 
 /*
+ * Forward over a packed batch of variable-length sequences ("Triton
+ * FlashAttention-2 forward", "Exercises": a cu_seqlens index packs requests of
+ * different lengths into one launch).  Sequence s occupies rows
+ * cu_seqlens[s] .. cu_seqlens[s+1]-1 of the packed tensors and attends only
+ * to itself (causal alignment relative to its own first token).
+ *   q, k, v    in : (total, H, D) bf16, packed
+ *   o          out: (total, H, D) bf16
+ *   lse        out: (H, total) float32
+ *   cu_seqlens in : DEVICE int32[n_seq + 1], cu_seqlens[0] = 0, non-decreasing,
+ *                   cu_seqlens[n_seq] = total (lengths may be 0)
+ *   max_seqlen    : an upper bound on every length (the caller knows it; the
+ *                   library does not read cu_seqlens on the host)
+ * A length above max_seqlen (or negative) is detected by the kernel and
+ * reported as FA_ERR_SEQLEN by fa_get_device_status; those outputs are invalid.
+ * Other arguments and errors as in fa_fwd.  No workspace.
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens, int n_seq, int max_seqlen, int total, int H, int D,
+                  float scale, int causal, void* stream);
+
+/*
  * Decoding forward, split over the keys ("Lab 06 - Attention kernels",
  * "Check yourself" item 2 and "Stretch": a few new query rows against a long
  * key/value cache).  Each of the Tq query rows of a head attends to ALL Tk
@@ -157,8 +179,8 @@ const char* fa_strerror(int status);
 
 /*
  * Synchronises `stream`, returns the device status word recorded by the
- * library's kernels on the current device since the last call (FA_OK or
- * FA_ERR_DEVICE_TIMEOUT), and clears it.  Returns FA_ERR_CUDA if the
+ * library's kernels on the current device since the last call (FA_OK,
+ * FA_ERR_DEVICE_TIMEOUT or FA_ERR_SEQLEN), and clears it.  Returns FA_ERR_CUDA if the
  * synchronisation itself fails.
  */
 int fa_get_device_status(void* stream);

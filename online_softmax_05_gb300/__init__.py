@@ -12,7 +12,7 @@ import math
 import os
 import threading
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "attention_decode", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen", "attention_forward_varlen", "fa_decode", "attention_decode", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
            "attention_forward", "attention_backward", "FAError", "library_path", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -23,7 +23,7 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_SHAPE", -3: "FA_ERR_UNSUPPORTED", -4: "FA_ERR_ALIGN",
                 -5: "FA_ERR_CUDA", -6: "FA_ERR_NOMEM", -7: "FA_ERR_DEVICE_TIMEOUT", -8: "FA_ERR_ARG",
-                -9: "FA_ERR_ARCH", -10: "FA_ERR_SCRATCH"}
+                -9: "FA_ERR_ARCH", -10: "FA_ERR_SCRATCH", -11: "FA_ERR_SEQLEN"}
 
 
 class FAError(RuntimeError):
@@ -55,6 +55,8 @@ def load_library():
         lib.fa_fwd_gqa.restype = i
         lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_bwd_gqa.restype = i
+        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_varlen.restype = i
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.fa_decode.restype = i
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -124,6 +126,35 @@ def fa_bwd_gqa(q, k, v, o, dO, lse, dq, dk, dv, B: int, Hq: int, Hkv: int, T: in
     """C-ABI ``fa_bwd_gqa``; dk, dv sum over each group of query heads."""
     return load_library().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
                                      _ptr(dv), B, Hq, Hkv, T, D, float(scale), int(causal), _stream(stream))
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, n_seq: int, max_seqlen: int, total: int, H: int, D: int,
+                  scale: float, causal: int, stream=None) -> int:
+    """C-ABI ``fa_fwd_varlen``: packed (total, H, D) sequences delimited by device cu_seqlens."""
+    return load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), n_seq,
+                                        max_seqlen, total, H, D, float(scale), int(causal), _stream(stream))
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale: float | None = None,
+                             out=None, lse=None, stream=None):
+    """O (total, H, D) and LSE (H, total) for packed sequences; cu_seqlens is an int32 CUDA tensor."""
+    import torch
+    total, H, D = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 3):
+            raise ValueError(f"{n} must be a contiguous (total, H, D) bf16 CUDA tensor")
+    if not (cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous()):
+        raise ValueError("cu_seqlens must be a contiguous int32 CUDA tensor")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total), device=q.device, dtype=torch.float32) if lse is None else lse
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_fwd_varlen(q, k, v, out, lse, cu_seqlens, cu_seqlens.numel() - 1, max_seqlen, total, H, D, scale,
+                       int(causal), stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_varlen")
+    return out, lse
 
 
 def fa_decode(q, k, v, o, lse, B: int, H: int, Tq: int, Tk: int, D: int, scale: float, stream=None) -> int:

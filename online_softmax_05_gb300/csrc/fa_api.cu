@@ -89,6 +89,7 @@ const char* fa_strerror(int status) {
         case FA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out (pipeline stall); outputs are invalid";
         case FA_ERR_ARG: return "causal must be 0 or 1, scale finite, and outputs must not overlap other buffers";
         case FA_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
+        case FA_ERR_SEQLEN: return "a cu_seqlens length is negative or above max_seqlen (recorded by the kernel)";
         case FA_ERR_SCRATCH: return "fa_bwd_noalloc: the problem needs more than the fixed 64 MiB scratch buffer";
         default: return "unknown fa_status";
     }
@@ -170,6 +171,31 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
                void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, int causal, void* stream) {
     return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, T, D, scale, causal, stream);
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens, int n_seq,
+                  int max_seqlen, int total, int H, int D, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o || !lse || !cu_seqlens) return FA_ERR_NULL;
+    if (n_seq < 1 || max_seqlen < 1 || total < 1 || H < 1) return FA_ERR_SHAPE;
+    if (static_cast<long long>(total) * H > INT_MAX || static_cast<long long>(n_seq) * H > (1 << 30))
+        return FA_ERR_SHAPE;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (causal != 0 && causal != 1) return FA_ERR_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+        return FA_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(total) * H * D * 2, nl = static_cast<size_t>(total) * H * 4;
+    const Range rq = range_of(q, n), rk = range_of(k, n), rv = range_of(v, n), ro = range_of(o, n),
+                rl = range_of(lse, nl), rc_ = range_of(cu_seqlens, static_cast<size_t>(n_seq + 1) * 4);
+    if (overlap(ro, rq) || overlap(ro, rk) || overlap(ro, rv) || overlap(ro, rl) || overlap(rl, rq) ||
+        overlap(rl, rk) || overlap(rl, rv) || overlap(ro, rc_) || overlap(rl, rc_))
+        return FA_ERR_ARG;
+    int dev = 0, sms = 0;
+    int rc = current_device(&dev, &sms);
+    if (rc != FA_OK) return rc;
+    return fa::launch_fwd_varlen(q, k, v, o, lse, cu_seqlens, n_seq, max_seqlen, total, H, D, scale, causal != 0,
+                                 static_cast<cudaStream_t>(stream), knobs(), sms);
 }
 
 int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Tq, int Tk, int D,

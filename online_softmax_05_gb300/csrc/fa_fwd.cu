@@ -89,6 +89,12 @@ struct FwdParams {
     float* lse;
     int T, BH, n_pairs, n_items;
     int Hq, Hkv, group;   // query heads, key/value heads, Hq / Hkv
+    // Packed variable-length batch: sequence s occupies rows cu_seqlens[s] ..
+    // cu_seqlens[s+1]-1 of (total, H, D) tensors (T above is then the longest
+    // length the caller promises; items past a sequence's end are skipped).
+    const int* cu_seqlens;
+    int n_seq, total;
+    __nv_bfloat16* o_packed;  // O of the packed layout (stored row by row, not by TMA)
     int head_pairs;       // 1: the two query tiles of an item are two heads of one group at the same rows
     int n_tiles;          // query tiles per head
     float sl2_eff;  // multiplier applied inside exp2: scale*log2e, or 1 when prescaled
@@ -141,13 +147,42 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) 
 // rows of two heads of one group ("Lab 06", "Check yourself" item 7: a K/V
 // tile loaded once serves several query heads).
 struct FwdItem {
-    int tile[2];  // query tile index of each half
-    int bh[2];    // batch * Hq + query head of each half
-    int bh_kv;    // batch * Hkv + key/value head
+    int tile[2];  // query tile index of each half (within its sequence)
+    int bh[2];    // head coordinate of each half's Q / O rows in the tensor maps
+    int bh_kv;    // head coordinate of the K/V rows
+    int T;        // length of this item's sequence
+    int row0;     // row coordinate of the sequence's first token (0 unless packed)
+    bool valid0;  // the first half has rows < T (false: skip the item)
     bool valid1;  // the second half has rows < T
 };
+template <bool VARLEN>
 __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     FwdItem it;
+    it.T = p.T;
+    it.row0 = 0;
+    it.valid0 = true;
+    if constexpr (VARLEN) {
+        // items: (pair of query tiles, sequence, head), heaviest pairs first
+        const int per_pair = p.n_seq * p.Hq;
+        const int pair = p.n_pairs - 1 - w / per_pair, rem = w % per_pair;
+        const int sq = rem / p.Hq, h = rem % p.Hq;
+        it.row0 = p.cu_seqlens[sq];
+        it.T = p.cu_seqlens[sq + 1] - it.row0;
+        it.tile[0] = 2 * pair;
+        it.tile[1] = 2 * pair + 1;
+        it.bh[0] = it.bh[1] = h;
+        it.bh_kv = h / p.group;
+        // a sequence that is longer than max_seqlen, negative, or outside the
+        // packed rows is skipped by every role alike and reported
+        const bool bad = it.T < 0 || it.T > p.T || it.row0 < 0 || it.row0 + it.T > p.total;
+        if (bad) {
+            atomicCAS(&g_status_fwd, 0, kStatusBadSeqlen);
+            it.T = 0;
+        }
+        it.valid0 = it.tile[0] * kFwdBM < it.T;
+        it.valid1 = it.tile[1] * kFwdBM < it.T;
+        return it;
+    }
     if (p.head_pairs) {
         const int per_t = p.BH / 2;  // head pairs over all batches
         const int t = p.n_tiles - 1 - w / per_t, rem = w % per_t;
@@ -176,7 +211,7 @@ __device__ __forceinline__ int item_of(int k, int n_items) {
     return w < n_items ? w : -1;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdParams p) {
@@ -241,10 +276,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int k = 0;; ++k) {
                 int w = item_of(k, p.n_items);
                 if (w < 0) break;
-                const FwdItem item = fwd_item(w, p);
+                const FwdItem item = fwd_item<VARLEN>(w, p);
+                if (!item.valid0) continue;
                 const bool valid1 = item.valid1;
-                const int n0 = fwd_num_kv_tiles(T, CAUSAL, item.tile[0]);
-                const int n1 = valid1 ? fwd_num_kv_tiles(T, CAUSAL, item.tile[1]) : 0;
+                const int n0 = fwd_num_kv_tiles(item.T, CAUSAL, item.tile[0]);
+                const int n1 = valid1 ? fwd_num_kv_tiles(item.T, CAUSAL, item.tile[1]) : 0;
                 const int nmax = n0 > n1 ? n0 : n1;
                 const int bh = item.bh_kv;
                 for (int t = 0; t < 2; ++t) {
@@ -253,9 +289,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     ++q_cnt[t];
                     mbar_arrive_expect_tx(q_full(t), C::kTileBytes);
                     ++q_armed[t];
+                    const int qrow = item.row0 + item.tile[t] * kFwdBM;
                     for (int a = 0; a < C::kAtoms; ++a)
                         tma_load_3d_hint(sQ[t] + a * C::kAtomBytes, &tm_q, q_full(t), 64 * a,
-                                         item.tile[t] * kFwdBM, item.bh[t], pol_q);
+                                         VARLEN ? item.bh[t] : qrow, VARLEN ? qrow : item.bh[t], pol_q);
                 }
                 for (int j = 0; j < nmax; ++j) {
                     for (int kind = 0; kind < 2; ++kind) {
@@ -269,9 +306,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         }
                         mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
                         const CUtensorMap* tm = kind ? &tm_v : &tm_k;
+                        const int krow = item.row0 + j * kBN;
                         for (int a = 0; a < C::kAtoms; ++a)
                             tma_load_3d_hint(sKV + slot * C::kTileBytes + a * C::kAtomBytes, tm, kv_full(slot),
-                                             64 * a, j * kBN, bh, pol_kv);
+                                             64 * a, VARLEN ? bh : krow, VARLEN ? krow : bh, pol_kv);
                     }
                 }
             }
@@ -314,10 +352,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int k = 0;; ++k) {
                 int w = item_of(k, p.n_items);
                 if (w < 0) break;
-                const FwdItem item = fwd_item(w, p);
+                const FwdItem item = fwd_item<VARLEN>(w, p);
+                if (!item.valid0) continue;
                 const bool valid1 = item.valid1;
-                const int n0 = fwd_num_kv_tiles(T, CAUSAL, item.tile[0]);
-                const int n1 = valid1 ? fwd_num_kv_tiles(T, CAUSAL, item.tile[1]) : 0;
+                const int n0 = fwd_num_kv_tiles(item.T, CAUSAL, item.tile[0]);
+                const int n1 = valid1 ? fwd_num_kv_tiles(item.T, CAUSAL, item.tile[1]) : 0;
                 const int nmax = n0 > n1 ? n0 : n1;
                 if (!wait_bar(q_full(0), q_cnt[0] & 1, ctl)) goto mma_done_label;
                 ++q_cnt[0];
@@ -396,10 +435,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int k = 0;; ++k) {
             int w = item_of(k, p.n_items);
             if (w < 0) break;
-            const FwdItem item = fwd_item(w, p);
-            const int tile = item.tile[t], bh = item.bh[t];
-            if (tile * kFwdBM >= T) continue;  // tile 1 of the last pair may be empty
-            const int row = tile * kFwdBM + r_local;
+            const FwdItem item = fwd_item<VARLEN>(w, p);
+            const int tile = item.tile[t], bh = item.bh[t], T = item.T;
+            if (tile * kFwdBM >= T) continue;  // the second tile of an item may be empty (or the whole item)
+            const int row = tile * kFwdBM + r_local;  // row within the sequence
             const int n = fwd_num_kv_tiles(T, CAUSAL, tile);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
@@ -502,7 +541,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!warp_wait(o_full(t), o_cnt & 1, ctl)) goto softmax_done;
             ++o_cnt;
             tc_fence_after();
-            {
+            if constexpr (VARLEN) {
+                // packed rows past this sequence's end belong to the next one: store row by row
+                const float inv = 1.f / l;
+                __nv_bfloat16* dst = p.o_packed + (static_cast<size_t>(item.row0 + row) * p.Hq + bh) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(tO + 32 * c, orr);
+                    tmem_ld_wait();
+                    reg_fence32(orr);
+                    if (row < T) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w4;
+                            w4.x = pack_bf16x2(__uint_as_float(orr[8 * q4 + 0]) * inv, __uint_as_float(orr[8 * q4 + 1]) * inv);
+                            w4.y = pack_bf16x2(__uint_as_float(orr[8 * q4 + 2]) * inv, __uint_as_float(orr[8 * q4 + 3]) * inv);
+                            w4.z = pack_bf16x2(__uint_as_float(orr[8 * q4 + 4]) * inv, __uint_as_float(orr[8 * q4 + 5]) * inv);
+                            w4.w = pack_bf16x2(__uint_as_float(orr[8 * q4 + 6]) * inv, __uint_as_float(orr[8 * q4 + 7]) * inv);
+                            reinterpret_cast<uint4*>(dst + 32 * c)[q4] = w4;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_bar(t));
+                if (wq == 0 && lane == 0) {
+                    wait_bar(epi_bar(t), epi_cnt & 1, ctl);
+                    mbar_arrive(q_empty(t));  // every S MMA reading this Q tile completed before o_full
+                }
+                ++epi_cnt;
+                if (row < T)
+                    p.lse[static_cast<size_t>(bh) * p.total + item.row0 + row] = (m_used + __log2f(l)) * kLn2;
+            } else {
                 const float inv = 1.f / l;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -552,11 +623,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN = false>
 int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                  const FwdParams& p, int grid, cudaStream_t st) {
     static bool attr_set = false;
-    auto kern = fa_fwd_kernel<D, CAUSAL>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmemBytes) !=
             cudaSuccess)
@@ -587,6 +658,10 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     p.n_pairs = cdiv(T, 2 * kFwdBM);
     p.head_pairs = (p.group % 2 == 0) ? 1 : 0;
     p.n_items = p.head_pairs ? p.n_tiles * (BH / 2) : p.n_pairs * BH;
+    p.cu_seqlens = nullptr;
+    p.n_seq = B;
+    p.total = B * T;
+    p.o_packed = nullptr;
     p.sl2 = scale * kLog2e;
     p.prescale = (p.sl2 > 0.f) ? 0 : 1;
     p.sl2_eff = p.prescale ? 1.f : p.sl2;
@@ -603,6 +678,40 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                     : launch_fwd_t<128, false>(tq, tk, tv, to, p, grid, stream);
     if (dbg.ev[1]) cudaEventRecord(dbg.ev[1], stream);
     return rc;
+}
+
+int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                      int n_seq, int max_seqlen, int total, int H, int D, float scale, bool causal,
+                      cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_packed(&tq, q, total, H, D, 128) || !make_tmap_packed(&tk, k, total, H, D, 128) ||
+        !make_tmap_packed(&tv, v, total, H, D, 128))
+        return -5;
+    FwdParams p;
+    p.lse = lse;
+    p.T = max_seqlen;
+    p.BH = H;
+    p.Hq = p.Hkv = H;
+    p.group = 1;
+    p.head_pairs = 0;
+    p.n_tiles = cdiv(max_seqlen, kFwdBM);
+    p.n_pairs = cdiv(max_seqlen, 2 * kFwdBM);
+    p.n_items = p.n_pairs * n_seq * H;
+    p.cu_seqlens = cu_seqlens;
+    p.n_seq = n_seq;
+    p.total = total;
+    p.o_packed = static_cast<__nv_bfloat16*>(o);
+    p.sl2 = scale * kLog2e;
+    p.prescale = (p.sl2 > 0.f) ? 0 : 1;
+    p.sl2_eff = p.prescale ? 1.f : p.sl2;
+    p.timeout_ns = dbg.timeout_ns;
+    p.inject = dbg.inject;
+    const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+    if (D == 64)
+        return causal ? launch_fwd_t<64, true, true>(tq, tk, tv, tq, p, grid, stream)
+                      : launch_fwd_t<64, false, true>(tq, tk, tv, tq, p, grid, stream);
+    return causal ? launch_fwd_t<128, true, true>(tq, tk, tv, tq, p, grid, stream)
+                  : launch_fwd_t<128, false, true>(tq, tk, tv, tq, p, grid, stream);
 }
 
 #ifdef FA_TRACE

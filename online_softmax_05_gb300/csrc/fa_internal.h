@@ -13,6 +13,7 @@ struct DebugKnobs {
 
 // Status word values written by kernels (mirror of fa_status).
 constexpr int kStatusTimeout = -7;
+constexpr int kStatusBadSeqlen = -11;
 
 // Launchers: arguments already validated by the C-ABI layer.
 // Hq query heads share Hkv key/value heads (Hq % Hkv == 0; Hkv == Hq is plain attention).
@@ -21,6 +22,11 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, bool causal,
                cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
+
+// Forward over a packed variable-length batch: (total, H, D) tensors, LSE (H, total).
+int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                      int n_seq, int max_seqlen, int total, int H, int D, float scale, bool causal,
+                      cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
 
 // Split-K decoding forward (fa_decode.cu).
 int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Tq, int Tk,

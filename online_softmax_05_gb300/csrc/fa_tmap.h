@@ -43,4 +43,23 @@ inline bool make_tmap_bhtd(CUtensorMap* map, const void* base, int BH, int T, in
     return r == CUDA_SUCCESS;
 }
 
+// Packed variable-length layout (total, H, D) bf16: dimensions (D, H, total)
+// with strides (2 B, D*2 B, H*D*2 B), boxes of 64 columns x 1 head x
+// box_rows rows.  The box lands in shared memory exactly as a
+// 64 x box_rows box of the (B*H, T, D) map does (rows of 128 bytes, 128-byte
+// swizzle), so kernels only swap the (row, head) coordinates.  Rows past
+// `total` read as zeros.
+inline bool make_tmap_packed(CUtensorMap* map, const void* base, int total, int H, int D, int box_rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(total)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+    cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_strerror_covers_codes(lib):
-    for code in range(0, -11, -1):
+    for code in range(0, -12, -1):
         s = fa.fa_strerror(code)
         assert s and "unknown" not in s
     assert "unknown" in fa.fa_strerror(-1234)
@@ -120,3 +120,21 @@ def test_argument_errors_gqa(lib):
     assert fa.fa_fwd_gqa(p[0], p[1], p[2], p[3], p[4], 1, 4, 0, 64, 128, 0.1, 0, None) == -2
     assert fa.fa_bwd_gqa(*p, 1, 4, 8, 64, 128, 0.1, 0, None) == -2                               # Hkv > Hq
     assert fa.fa_bwd_gqa(*p[:8], None, 1, 4, 2, 64, 128, 0.1, 0, None) == -1
+
+
+def test_argument_errors_varlen(lib):
+    base = 0x1000_0000
+    q, k, v, o, lse, cu = (base * (i + 1) for i in range(6))
+    f = lambda **kw: fa.fa_fwd_varlen(kw.get("q", q), k, v, kw.get("o", o), lse, kw.get("cu", cu),
+                                      kw.get("n_seq", 3), kw.get("max_seqlen", 100), kw.get("total", 250), 2,
+                                      kw.get("D", 128), kw.get("scale", 0.1), kw.get("causal", 1), None)
+    assert f(cu=None) == -1
+    assert f(n_seq=0) == -2
+    assert f(max_seqlen=0) == -2
+    assert f(total=0) == -2
+    assert f(D=80) == -3
+    assert f(causal=2) == -8
+    assert f(scale=float("inf")) == -8
+    assert f(cu=cu + 2) == -4
+    assert f(q=base + 8) == -4
+    assert f(o=k) == -8
