@@ -43,7 +43,8 @@ CLOCK_FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["online_softmax_05_gb300/csrc/fa_fwd.cu"],
-    "fa_bwd_main_kernel": ["online_softmax_05_gb300/csrc/fa_bwd.cu"],
+    "fa_bwd_dkdv_kernel": ["online_softmax_05_gb300/csrc/fa_bwd.cu"],
+    "fa_bwd_dq_kernel": ["online_softmax_05_gb300/csrc/fa_bwd.cu"],
 }
 COMMON_SOURCES = ["online_softmax_05_gb300/csrc/fa_ptx.cuh", "online_softmax_05_gb300/csrc/fa_sched.h",
                   "online_softmax_05_gb300/csrc/fa_tmap.h"]
@@ -460,9 +461,9 @@ def main():
     if fa.fa_get_device_status(stream) != 0:
         raise RuntimeError("device status reported a stalled kernel during warm-up")
 
-    # per-step events around the forward kernel and the backward's main kernel
+    # per-step events around the forward kernel and the backward's two main kernels
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     for e4 in evs:
         for e in e4:
             e.record(stream)
@@ -484,7 +485,7 @@ def main():
             step()
         t_end.record(stream)
         torch.cuda.synchronize(dev)
-    lib.fa_set_timing_events(None, None, None, None)
+    lib.fa_set_timing_events(None, None, None, None, None)
     if dist is not None:
         dist.barrier()
     status = fa.fa_get_device_status(stream)
@@ -492,17 +493,25 @@ def main():
         raise RuntimeError(f"device status {status} after the timed region")
     ms = t_start.elapsed_time(t_end) / K
     fwd_ms = statistics.mean(evs[s][0].elapsed_time(evs[s][1]) for s in range(K))
-    bwd_ms = statistics.mean(evs[s][2].elapsed_time(evs[s][3]) for s in range(K))
+    dkdv_ms = statistics.mean(evs[s][2].elapsed_time(evs[s][3]) for s in range(K))
+    dq_ms = statistics.mean(evs[s][3].elapsed_time(evs[s][4]) for s in range(K))
     if dist is not None:
-        tt = torch.tensor([ms, fwd_ms, bwd_ms], device=dev, dtype=torch.float64)
+        tt = torch.tensor([ms, fwd_ms, dkdv_ms, dq_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, fwd_ms, bwd_ms = tt.tolist()
+        ms, fwd_ms, dkdv_ms, dq_ms = tt.tolist()
+    bwd_ms = dkdv_ms + dq_ms
 
     fwd_fl, bwd_fl = workload_flops(w, causal)
     step_fl = fwd_fl + bwd_fl
     value = world * step_fl / (ms * 1e-3) / 1e12
     fwd_tflops_kernel = fwd_fl / (fwd_ms * 1e-3) / 1e12
-    bwd_tflops_kernel = bwd_fl / (bwd_ms * 1e-3) / 1e12
+    bwd_tflops_kernels = bwd_fl / (bwd_ms * 1e-3) / 1e12
+    # Algorithmic FLOPs per backward kernel: of the backward's five products
+    # (S, dP, dV, dK, dQ; 2.5x the forward) the dK/dV kernel performs four
+    # (2x the forward) and the dQ kernel one (0.5x); the dQ kernel's
+    # recomputation of S and dP is extra work and is not counted.
+    dkdv_tflops = 2.0 * fwd_fl / (dkdv_ms * 1e-3) / 1e12
+    dq_tflops = 0.5 * fwd_fl / (dq_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak_sus, peak_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
 
@@ -511,9 +520,9 @@ def main():
                 "frac": achieved / peak_sus, "peak_kind": f"bf16 dense, sustained, of {peak_src}",
                 "frac_of_burst": achieved / peak_burst, "traffic": recorded_traffic(kernel, w.name)}
 
-    dominant_bwd = bwd_ms >= fwd_ms
-    rl_bwd = roofline("fa_bwd_main_kernel", bwd_tflops_kernel)
-    rl_fwd = roofline("fa_fwd_kernel", fwd_tflops_kernel)
+    rls = sorted([(fwd_ms, roofline("fa_fwd_kernel", fwd_tflops_kernel)),
+                  (dkdv_ms, roofline("fa_bwd_dkdv_kernel", dkdv_tflops)),
+                  (dq_ms, roofline("fa_bwd_dq_kernel", dq_tflops))], key=lambda x: -x[0])
 
     # end to end through the public API with host buffers (pinned), copies timed
     e2e = None
@@ -571,12 +580,13 @@ def main():
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "causal": causal,
                    "passes": "fwd+bwd", "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: inputs + outputs + workspace per step ~0.7 GB > 129 MB L2"},
-        "fwd_tflops": fwd_tflops_kernel, "fwd_ms": fwd_ms, "bwd_main_ms": bwd_ms,
+        "fwd_tflops": fwd_tflops_kernel, "fwd_ms": fwd_ms, "bwd_dkdv_ms": dkdv_ms, "bwd_dq_ms": dq_ms,
+        "bwd_tflops": bwd_tflops_kernels,
         "pct_of_peak": {"fwd_bwd_of_burst": 100 * value / world / peak_burst,
                         "fwd_bwd_of_sustained": 100 * value / world / peak_sus,
                         "fwd_of_burst": 100 * fwd_tflops_kernel / peak_burst, "peaks": peak_src},
-        "roofline": rl_bwd if dominant_bwd else rl_fwd,
-        "roofline_other": rl_fwd if dominant_bwd else rl_bwd,
+        "roofline": rls[0][1],
+        "roofline_other": [r for _, r in rls[1:]],
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * K,
         "clocks": clocks.summary(),
     }

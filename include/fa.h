@@ -26,9 +26,9 @@
  *
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream).  Calls are asynchronous: they enqueue kernels on `stream` and
- * return without synchronising.  fa_bwd takes its workspace (B*H*T floats for
- * D, B*H*T*D floats for the dQ accumulator, B*H*T_pad floats for log2-scaled
- * LSE) stream-ordered with cudaMallocAsync on `stream` and releases it with
+ * return without synchronising.  fa_bwd takes its workspace (two vectors of
+ * B*H*T_pad floats, T_pad = T rounded up to 128: D and log2-scaled LSE)
+ * stream-ordered with cudaMallocAsync on `stream` and releases it with
  * cudaFreeAsync on the same stream before returning.
  *
  * Errors.  Every entry point validates its arguments before launching
@@ -79,7 +79,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   dq, dk, dv     out: (B, H, T, D) bf16 gradients of sum(dO o O) with
  *                       respect to q, k, v (overwritten, not accumulated)
  *   B, H, T, D, scale, causal: as in fa_fwd.
- * dq is accumulated in float32 across key tiles and rounded to bf16 once.
+ * dq is accumulated in float32 across key tiles (in one kernel that walks the
+ * key tiles of each query tile) and rounded to bf16 once; no global-memory
+ * reductions are involved, so the result is deterministic.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, void* dq, void* dk, void* dv,
@@ -98,15 +100,14 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  *
  * Same arguments, layout, results and asynchrony as fa_bwd.  The caller
  * still owns every input and output.
- * Limit: 8 * B*H*T_pad + 4 * B*H*T*D bytes must not exceed the scratch size,
- *   where T_pad is T rounded up to a multiple of 128 (roughly
- *   B*H*T*D <= 16 M elements at D = 128); larger problems return
- *   FA_ERR_SCRATCH and nothing is enqueued.
+ * Limit: 8 * B*H*T_pad bytes must not exceed the scratch size, where T_pad
+ *   is T rounded up to a multiple of 128 (B*H*T_pad <= 8 M rows); larger
+ *   problems return FA_ERR_SCRATCH and nothing is enqueued.
  * Set-up: the first call on each device looks up the buffer's device
  *   address (cudaGetSymbolAddress); make that first call before any stream
  *   capture.
  * Sharing: every call uses the same buffer, which keeps the previous call's
- *   contents (the backward clears what must start at zero).  Calls whose
+ *   contents (the backward rewrites all of it before reading it).  Calls whose
  *   work overlaps on the GPU (different streams, or different host threads
  *   without ordering) race on the buffer and corrupt each other's results;
  *   serialise them.
@@ -224,12 +225,13 @@ int fa_debug_inject(int mode);
  * Measurement hook (default off; host state read by each call).  When the
  * pointers are non-NULL, later calls record these CUDA events (cudaEvent_t
  * passed as void*, created and owned by the caller) on the call's stream:
- * fwd_begin / fwd_end immediately around the forward kernel, bwd_begin /
- * bwd_end immediately around the backward's main kernel (not its
- * preprocess or dQ conversion).  Pass NULLs to turn it off.  Used to time
- * the dominant kernel inside a timed region without a profiler.
+ * fwd_begin / fwd_end immediately around the forward kernel; bwd_begin
+ * before the backward's dK/dV kernel, bwd_mid between it and the dQ kernel,
+ * bwd_end after the dQ kernel (the preprocess is outside).  Pass NULLs to
+ * turn it off.  Used to time the dominant kernels inside a timed region
+ * without a profiler.
  */
-int fa_set_timing_events(void* fwd_begin, void* fwd_end, void* bwd_begin, void* bwd_end);
+int fa_set_timing_events(void* fwd_begin, void* fwd_end, void* bwd_begin, void* bwd_mid, void* bwd_end);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,7 @@ namespace {
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject{0};
-std::atomic<void*> g_events[4] = {nullptr, nullptr, nullptr, nullptr};
+std::atomic<void*> g_events[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_dev_once[kMaxDevices];
@@ -67,7 +67,7 @@ int current_device(int* dev_out, int* sms_out) {
 
 fa::DebugKnobs knobs() {
     fa::DebugKnobs k{g_timeout_ns.load(), g_inject.load(), {}};
-    for (int i = 0; i < 4; ++i) k.ev[i] = static_cast<cudaEvent_t>(g_events[i].load());
+    for (int i = 0; i < 5; ++i) k.ev[i] = static_cast<cudaEvent_t>(g_events[i].load());
     return k;
 }
 
@@ -293,11 +293,12 @@ int fa_debug_set_wait_timeout_ns(unsigned long long ns) {
     return FA_OK;
 }
 
-int fa_set_timing_events(void* fwd_begin, void* fwd_end, void* bwd_begin, void* bwd_end) {
+int fa_set_timing_events(void* fwd_begin, void* fwd_end, void* bwd_begin, void* bwd_mid, void* bwd_end) {
     g_events[0].store(fwd_begin);
     g_events[1].store(fwd_end);
     g_events[2].store(bwd_begin);
-    g_events[3].store(bwd_end);
+    g_events[3].store(bwd_mid);
+    g_events[4].store(bwd_end);
     return FA_OK;
 }
 

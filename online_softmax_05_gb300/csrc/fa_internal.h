@@ -8,12 +8,13 @@ namespace fa {
 struct DebugKnobs {
     unsigned long long timeout_ns;  // bound of every in-kernel wait
     int inject;                     // fault-injection mode (0 = off)
-    cudaEvent_t ev[4];              // measurement hook: fwd begin/end, bwd-main begin/end (may be null)
+    cudaEvent_t ev[5];              // measurement hook: fwd begin/end; bwd: before dK/dV, between, after dQ (may be null)
 };
 
 // Status word values written by kernels (mirror of fa_status).
 constexpr int kStatusTimeout = -7;
 constexpr int kStatusBadSeqlen = -11;
+constexpr int kStatusSmemAlign = -4;  // a kernel's dynamic shared-memory window was not 1024-byte aligned
 
 // Launchers: arguments already validated by the C-ABI layer.
 // Hq query heads share Hkv key/value heads (Hq % Hkv == 0; Hkv == Hq is plain attention).

@@ -171,100 +171,69 @@ __global__ void __launch_bounds__(128, 1)
         for (int i = threadIdx.x; i < bytes; i += blockDim.x) dst[i] = smem[i];
 }
 
-// Issue-rate probe: one thread issues `n` back-to-back 128xNx16 bf16 MMAs
-// (SS, K-major) into one accumulator; cycles to issue them and until the
-// commit lands are written to out[0], out[1].  mode 0: descriptors built per
-// MMA from the shared address; mode 1: descriptors precomputed, 64-bit add
-// per step; mode 2: as mode 1, then the latency of a try_wait on an
-// already completed mbarrier phase is written to out[2].  Operand contents
-// are whatever shared memory holds (not checked).
-__global__ void __launch_bounds__(128, 1) probe_mma_rate_kernel(int N, int n, int mode, long long* out, int* err) {
+// Issues n_chains chains of CHAIN back-to-back MMAs (unrolled: the issuing
+// thread must spend far less than an MMA per instruction).
+template <int CHAIN>
+__device__ __forceinline__ void chain_issue(int kind, int n_chains, uint32_t tmem, uint64_t da, uint64_t db, bool bmn,
+                                            uint32_t idesc) {
+    const uint64_t bstep = bmn ? 128u : 2u;
+    for (int c = 0; c < n_chains; ++c) {
+        const uint32_t acc = tmem + ((c & 1) ? 128u : 0u);
+        if (kind == 2) {
+#pragma unroll
+            for (int s = 0; s < CHAIN; ++s) mma_ts(acc, tmem + 384u + (s & 3) * 8, db + (s & 3) * bstep, idesc, s > 0);
+        } else {
+#pragma unroll
+            for (int s = 0; s < CHAIN; ++s) mma_ss(acc, da + (s & 3) * 2, db + (s & 3) * bstep, idesc, s > 0);
+        }
+    }
+}
+
+// Cost of tcgen05.mma chains: n instructions of 128 x N x 16 split into
+// chains of `chain` instructions, each chain accumulating into one of two
+// TMEM accumulators (they alternate chain by chain).  kind 0: A and B
+// K-major in smem; 1: A K-major, B MN-major; 2: A from TMEM, B MN-major.
+// Cycles from the first issue to the completion of the last are written to out[0].
+__global__ void __launch_bounds__(128, 1) probe_mma_chain_kernel(int N, int n, int chain, int kind, long long* out,
+                                                                 int* err) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint32_t sA = smem_u32(smem);
-    uint32_t sB = sA + 128 * 64 * 2;
-    uint32_t bar = sB + 256 * 64 * 2;
-    uint32_t tslot = bar + 8;
-    int tid = threadIdx.x, warp = tid >> 5;
-    for (int i = tid; i < (128 + 256) * 64 * 2 / 4; i += 128) reinterpret_cast<uint32_t*>(smem)[i] = 0x3f803f80u;
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + 128 * 64 * 2;           // 16 KB of A (K-major, 4 k-steps per 128-byte row)
+    const uint32_t bar = sB + 2 * 128 * 128;         // 32 KB of B (two 64-wide atoms of 128 rows)
+    const uint32_t tslot = bar + 8;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int i = tid; i < (128 * 64 * 2 + 2 * 128 * 128) / 4; i += 128) reinterpret_cast<uint32_t*>(smem)[i] = 0x3f803f80u;
     if (warp == 0) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
         mbar_init(bar, 1);
-        mbar_init(bar + 16, 1);
         fence_mbar_init();
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tslot - sA));
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tslot - sA));
     if (tid == 0) {
-        mbar_arrive(bar + 16);
-        const uint32_t idesc = idesc_bf16_f32(128, N, false, false);
-        long long t0 = clock64();
-        if (mode == 0) {
-            for (int i = 0; i < n; ++i) {
-                const int s = i & 3;
-                mma_ss(tmem, sdesc_sw128(sA + s * 32, 16, 1024), sdesc_sw128(sB + s * 32, 16, 1024), idesc, i > 0);
-            }
-        } else if (mode <= 2) {
-            const uint64_t da = sdesc_sw128(sA, 16, 1024), db = sdesc_sw128(sB, 16, 1024);
-            for (int i = 0; i < n; ++i) {
-                const uint64_t off = static_cast<uint64_t>((i & 3) * 2);
-                mma_ss(tmem, da + off, db + off, idesc, i > 0);
-            }
-        } else if (mode >= 8) {
-            // 8: TS B-MN, 9: SS A-MN B-MN, 10: TS B-K, 11: SS K/K -- alternating between two
-            // independent accumulators (columns 0 and 256 - N; two chains in flight)
-            const bool ts = (mode == 8 || mode == 10), amn = (mode == 9), bmn = (mode == 8 || mode == 9);
-            const uint32_t id2 = idesc_bf16_f32(128, N, amn, bmn);
-            const uint64_t da = amn ? sdesc_sw128(sA, 64 * 128, 1024) : sdesc_sw128(sA, 16, 1024);
-            const uint64_t db = bmn ? sdesc_sw128(sB, 64 * 128, 1024) : sdesc_sw128(sB, 16, 1024);
-            const uint32_t acc2 = tmem + 256u;
-            for (int i = 0; i < n; ++i) {
-                const int k = i >> 1;
-                const uint64_t offa = amn ? static_cast<uint64_t>((k & 3) * 128) : static_cast<uint64_t>((k & 3) * 2);
-                const uint64_t offb = bmn ? static_cast<uint64_t>((k & 3) * 128) : static_cast<uint64_t>((k & 3) * 2);
-                const uint32_t d = (i & 1) ? acc2 - (ts ? 0u : 0u) : tmem;
-                if (ts)
-                    mma_ts((i & 1) ? tmem + 128u : tmem, tmem + 384u + (k & 3) * 8, db + offb, id2, i > 1);
-                else
-                    mma_ss((i & 1) ? tmem + 256u : d, da + offa, db + offb, id2, i > 1);
-            }
-        } else {
-            // mode 3: A MN-major, 4: B MN-major, 5: both MN-major, 6: A from TMEM (B K-major),
-            // 7: A from TMEM with B MN-major
-            const bool amn = (mode == 3 || mode == 5), bmn = (mode == 4 || mode == 5 || mode == 7);
-            const uint32_t id2 = idesc_bf16_f32(128, N, amn, bmn);
-            const uint64_t da = amn ? sdesc_sw128(sA, 64 * 128, 1024) : sdesc_sw128(sA, 16, 1024);
-            const uint64_t db = bmn ? sdesc_sw128(sB, 64 * 128, 1024) : sdesc_sw128(sB, 16, 1024);
-            for (int i = 0; i < n; ++i) {
-                const uint64_t offa = amn ? static_cast<uint64_t>((i & 3) * 128) : static_cast<uint64_t>((i & 3) * 2);
-                const uint64_t offb = bmn ? static_cast<uint64_t>((i & 3) * 128) : static_cast<uint64_t>((i & 3) * 2);
-                if (mode >= 6)
-                    mma_ts(tmem, tmem + 256u + (i & 3) * 8, db + offb, id2, i > 0);
-                else
-                    mma_ss(tmem, da + offa, db + offb, id2, i > 0);
-            }
-        }
-        long long t1 = clock64();
-        long long t3 = 0;
-        if (mode == 2) {
-            // latency of waiting on an mbarrier phase that completed before the MMAs were issued
-            const uint32_t bar2 = bar + 16;
-            const bool ok = mbar_try_wait(bar2, 0);
-            t3 = clock64() - t1;
-            if (!ok) atomicExch(err, 2);
+        const bool bmn = kind != 0;
+        const uint32_t idesc = idesc_bf16_f32(128, N, false, bmn);
+        const uint64_t da = sdesc_sw128(sA, 16, 1024);
+        const uint64_t db = bmn ? sdesc_sw128(sB, 128 * 128, 1024) : sdesc_sw128(sB, 16, 1024);
+        const long long t0 = clock64();
+        switch (chain) {
+            case 1: chain_issue<1>(kind, n / 1, tmem, da, db, bmn, idesc); break;
+            case 2: chain_issue<2>(kind, n / 2, tmem, da, db, bmn, idesc); break;
+            case 4: chain_issue<4>(kind, n / 4, tmem, da, db, bmn, idesc); break;
+            case 8: chain_issue<8>(kind, n / 8, tmem, da, db, bmn, idesc); break;
+            case 16: chain_issue<16>(kind, n / 16, tmem, da, db, bmn, idesc); break;
+            default: chain_issue<32>(kind, n / 32, tmem, da, db, bmn, idesc); break;
         }
         mma_commit(bar);
         probe_wait(bar, 0, err);
-        long long t2 = clock64();
-        out[0] = t1 - t0;
-        out[1] = t2 - t0;
-        out[2] = t3;
+        out[0] = clock64() - t0;
     }
     __syncwarp();
     tc_fence_before();
@@ -324,21 +293,23 @@ int probe_exp2_rate(int mode, int iters, int warps, long long* out_host, float* 
 }
 
 
-int probe_mma_rate(int N, int n, int mode, long long* out_host) {
-    if (!(N == 64 || N == 128 || N == 256) || n < 1 || n > 4096) return -1;
+int probe_mma_chain(int N, int n, int chain, int kind, long long* out_host) {
+    if (!(N == 64 || N == 128) || n < 1 || n > 4096 || !(chain == 1 || chain == 2 || chain == 4 || chain == 8 ||
+                                                        chain == 16 || chain == 32) ||
+        n % chain || kind < 0 || kind > 2)
+        return -1;
     int* err = nullptr;
     long long* out = nullptr;
     if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) return -5;
-    if (cudaMalloc(&out, 3 * sizeof(long long)) != cudaSuccess) return -5;
+    if (cudaMalloc(&out, sizeof(long long)) != cudaSuccess) return -5;
     cudaMemset(err, 0, sizeof(int));
-    int smem = 1024 + (128 + 256) * 64 * 2 + 64;
-    if (mode < 0 || mode > 11) return -1;
-    cudaFuncSetAttribute(fa::probe_mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    fa::probe_mma_rate_kernel<<<1, 128, smem>>>(N, n, mode, out, err);
+    const int smem = 1024 + 128 * 64 * 2 + 2 * 128 * 128 + 64;
+    cudaFuncSetAttribute(fa::probe_mma_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    fa::probe_mma_chain_kernel<<<1, 128, smem>>>(N, n, chain, kind, out, err);
     cudaError_t e = cudaDeviceSynchronize();
     int h = 0;
     cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost);
-    cudaMemcpy(out_host, out, 3 * sizeof(long long), cudaMemcpyDeviceToHost);
+    cudaMemcpy(out_host, out, sizeof(long long), cudaMemcpyDeviceToHost);
     cudaFree(err);
     cudaFree(out);
     if (e != cudaSuccess) return -5;

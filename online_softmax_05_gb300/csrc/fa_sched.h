@@ -21,9 +21,10 @@ namespace fa {
 constexpr int kFwdBM = 128;  // forward query tile rows (one TMEM lane per row)
 constexpr int kBN = 128;     // key tile rows, forward and backward
 
-// Backward query tile rows: 64 at D = 128 (TMEM holds two S/dP buffers plus
-// dK, dV), 128 at D = 64.
-FA_HD constexpr int bwd_bm(int D) { return D == 128 ? 64 : 128; }
+// Backward query tile rows: 128 at both head sizes.  The transposed-operand
+// MMAs of the backward cost a fixed ~118 cycles per instruction up to N = 128,
+// so 128-row query tiles halve their count per unit of work.
+FA_HD constexpr int bwd_bm(int /*D*/) { return 128; }
 
 FA_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
 FA_HD int imin(int a, int b) { return a < b ? a : b; }

@@ -85,7 +85,7 @@ def test_argument_errors_bwd(lib):
 def test_tile_rows(lib):
     a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     assert lib.fa_sched_tile_rows(128, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)) == 0
-    assert (a.value, b.value, c.value) == (128, 128, 64)
+    assert (a.value, b.value, c.value) == (128, 128, 128)
     assert lib.fa_sched_tile_rows(64, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)) == 0
     assert (a.value, b.value, c.value) == (128, 128, 128)
     assert lib.fa_sched_tile_rows(80, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)) == -3

@@ -72,26 +72,27 @@ def test_tma_probe_swizzle_and_zero_fill(plib, D, row0, bh):
 
 
 @pytest.mark.gpu
-def test_mma_issue_rate_report(plib, capsys):
-    """Issue/complete rate of 128xNx16 bf16 tcgen05.mma chains by operand form.
-
-    Prints the table summarised in profiles/tcgen05_mma_issue_rates.md and
-    checks the dense K-major SS form runs within 30 % of 8192 FLOP/clk at N >= 128."""
-    plib.probe_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong)]
-    names = {1: "SS, A and B K-major", 4: "SS, B MN-major", 5: "SS, A and B MN-major", 6: "TS (A in TMEM), B K-major",
-             7: "TS, B MN-major", 11: "SS K-major, 2 accumulators alternating",
-             9: "SS MN-major, 2 accumulators alternating", 8: "TS B MN-major, 2 accumulators alternating"}
+def test_mma_chain_length_report(plib, capsys):
+    """Cycles per 128xNx16 bf16 tcgen05.mma when n = 256 instructions run as
+    chains of `chain` instructions on one accumulator, alternating between two
+    accumulators chain by chain (the shape of the attention kernels' products:
+    a chain per product, K / 16 instructions long).  Checks the long chains
+    of the dense K-major form stream within 30 % of 8192 FLOP/clk."""
+    plib.probe_mma_chain.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_longlong)]
+    kinds = {0: "SS, A and B K-major", 1: "SS, A K-major, B MN-major", 2: "TS (A in TMEM), B MN-major"}
     rows = []
-    for N in (64, 128, 256):
-        for mode in names:
-            o = (ctypes.c_longlong * 3)()
-            assert plib.probe_mma_rate(N, 256, mode, o) == 0
-            assert plib.probe_mma_rate(N, 256, mode, o) == 0
-            rows.append((N, names[mode], o[1] / 256.0, 128 * N * 16 * 2 / 8192))
+    for N in (64, 128):
+        for kind in kinds:
+            for chain in (1, 2, 4, 8, 16, 32):
+                o = (ctypes.c_longlong * 1)()
+                assert plib.probe_mma_chain(N, 256, chain, kind, o) == 0
+                assert plib.probe_mma_chain(N, 256, chain, kind, o) == 0
+                rows.append((N, kinds[kind], chain, o[0] / 256.0))
     with capsys.disabled():
-        print("\n  N  form                                       cycles/MMA  ideal")
-        for N, name, c, ideal in rows:
-            print(f"{N:4d}  {name:42s} {c:9.1f} {ideal:6.0f}")
-    for N, name, c, ideal in rows:
-        if name == "SS, A and B K-major" and N >= 128:
-            assert c <= 1.3 * ideal
+        print("\n  N  form                          chain  cycles/MMA")
+        for N, name, chain, c in rows:
+            print(f"{N:4d}  {name:28s} {chain:6d} {c:10.1f}")
+    for N, name, chain, c in rows:
+        if N == 128 and name == kinds[0] and chain == 32:
+            assert c <= 1.3 * 64

@@ -58,9 +58,9 @@ def test_noalloc_matches_fa_bwd_on_two_calls(lib, B, H, T, D, causal):
 
 @pytest.mark.gpu
 def test_noalloc_refuses_problems_larger_than_its_scratch(lib):
-    # 2 x 16 x 8192 x 128 needs ~130 MB of scratch: refused before any launch
-    base = 1 << 32
+    # 64 x 32 x 8192 rows need 128 MiB of scratch (8 bytes a row): refused before any launch
+    base = 1 << 40
     ptrs = [base * (i + 1) for i in range(9)]
-    rc = lib.fa_bwd_noalloc(*ptrs, 2, 16, 8192, 128, 0.088, 1, None)
+    rc = lib.fa_bwd_noalloc(*ptrs, 64, 32, 8192, 128, 0.088, 1, None)
     assert rc == -10
     assert "scratch" in fa.fa_strerror(rc)
