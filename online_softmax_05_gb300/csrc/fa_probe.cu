@@ -241,6 +241,95 @@ __global__ void __launch_bounds__(128, 1) probe_mma_chain_kernel(int N, int n, i
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Sequences of 8-instruction chains shaped like the attention kernels' loops
+// (128 x 128 x 16 bf16 MMAs; n_iter iterations of three chains each):
+//   mode 0  SS, SS, SS chains into three accumulators (columns 0, 128, 256)
+//   mode 1  mode 0 plus a tcgen05.commit to an mbarrier after every chain
+//   mode 2  mode 1 plus, before every chain, a try_wait on an mbarrier phase
+//           that has already completed and a tcgen05 fence (what the kernels
+//           do when an operand is already there)
+//   mode 3  the dQ kernel's loop: SS (dP, columns 256), TS with A from
+//           columns 32.. of the S buffer (dQ, columns 384), SS (S, columns
+//           0 / 128 alternating), commits and waits as in mode 2
+// Cycles from the first issue to the completion of the last MMA go to out[0].
+__global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_iter, long long* out, int* err) {
+    out += blockIdx.x;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + 128 * 128 * 2;          // A: 128 rows x 128 K (two 64-wide atoms), 32 KB
+    const uint32_t bar = sB + 128 * 128 * 2;         // B: 128 rows x 128 (two atoms), 32 KB
+    const uint32_t bar2 = bar + 8, bar3 = bar + 16;
+    const uint32_t tslot = bar + 24;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int i = tid; i < (2 * 128 * 128 * 2) / 4; i += 128) reinterpret_cast<uint32_t*>(smem)[i] = 0x3f803f80u;
+    if (warp == 0) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init(bar2, 1);
+        mbar_init(bar3, 1);
+        fence_mbar_init();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tslot - sA));
+    if (tid == 0) {
+        mbar_arrive(bar3);  // a phase that has completed: waits on it return at once
+        const uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
+        const uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);
+        const SDesc dA = sdesc_make(sA, 16, 1024), dB = sdesc_make(sB, 16, 1024);
+        const SDesc dBmn = sdesc_make(sB, 128 * 128, 1024);
+        auto chain_ss = [&](uint32_t acc) {
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4;
+                mma_ss_d(acc, dA, off, dB, off, id_kk, s > 0);
+            }
+        };
+        auto chain_ts = [&](uint32_t acc, uint32_t a_col) {
+#pragma unroll
+            for (int s = 0; s < 8; ++s) mma_ts_d(acc, a_col + s * 8, dBmn, s * (2048 >> 4), id_mn, 1u);
+        };
+        auto between = [&]() {
+            if (mode >= 1) mma_commit(bar2);
+            if (mode >= 2) {
+                if (!mbar_try_wait(bar3, 0)) atomicExch(err, 3);
+                tc_fence_after();
+            }
+        };
+        const long long t0 = clock64();
+        for (int it = 0; it < n_iter; ++it) {
+            if (mode <= 2) {
+                chain_ss(tmem + 0);
+                between();
+                chain_ss(tmem + 128);
+                between();
+                chain_ss(tmem + 256);
+                between();
+            } else {
+                chain_ss(tmem + 256);
+                between();
+                chain_ts(tmem + 384, tmem + (it & 1) * 128 + 32);
+                between();
+                chain_ss(tmem + (it & 1) * 128);
+                between();
+            }
+        }
+        mma_commit(bar);
+        probe_wait(bar, 0, err);
+        out[0] = clock64() - t0;
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // Throughput of exp2: mode 0 = ex2.approx (MUFU), mode 1 = polynomial on
 // the FMA/ALU pipes (round-to-nearest by the 1.5*2^23 add, degree-3
 // least-squares fit of 2^f on [-1/2, 1/2], integer add into the exponent).
@@ -316,6 +405,29 @@ int probe_mma_chain(int N, int n, int chain, int kind, long long* out_host) {
     return h ? -7 : 0;
 }
 
+
+// ctas: number of CTAs (one per SM at this shared-memory size) running the
+// same sequence at once; out_host receives one count per CTA.
+int probe_mma_seq(int mode, int n_iter, int ctas, long long* out_host) {
+    if (mode < 0 || mode > 3 || n_iter < 1 || n_iter > 4096 || ctas < 1 || ctas > 1024) return -1;
+    int* err = nullptr;
+    long long* out = nullptr;
+    if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) return -5;
+    if (cudaMalloc(&out, ctas * sizeof(long long)) != cudaSuccess) return -5;
+    cudaMemset(err, 0, sizeof(int));
+    // more than half of the SM's shared memory: at most one CTA per SM
+    const int smem = 120 * 1024;
+    cudaFuncSetAttribute(fa::probe_mma_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    fa::probe_mma_seq_kernel<<<ctas, 128, smem>>>(mode, n_iter, out, err);
+    cudaError_t e = cudaDeviceSynchronize();
+    int h = 0;
+    cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaMemcpy(out_host, out, ctas * sizeof(long long), cudaMemcpyDeviceToHost);
+    cudaFree(err);
+    cudaFree(out);
+    if (e != cudaSuccess) return -5;
+    return h ? -7 : 0;
+}
 
 int probe_mma(int a_mode, int b_mode, int N, int K, const void* A, const void* B, float* out) {
     if (a_mode < 0 || a_mode > 2 || b_mode < 0 || b_mode > 1) return -1;

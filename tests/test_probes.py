@@ -96,3 +96,28 @@ def test_mma_chain_length_report(plib, capsys):
     for N, name, chain, c in rows:
         if N == 128 and name == kinds[0] and chain == 32:
             assert c <= 1.3 * 64
+
+
+@pytest.mark.gpu
+def test_mma_sequence_report(plib, capsys):
+    """Cycles per 128x128x16 MMA for loops of three 8-instruction chains shaped
+    like the attention kernels' (see probe_mma_seq_kernel): plain, with a
+    commit after each chain, with commit + satisfied wait + fence, and the
+    dQ kernel's SS / TS / SS rotation; on one SM and on every SM at once."""
+    import torch
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    plib.probe_mma_seq.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong)]
+    names = {0: "3 accumulators, SS chains", 1: "+ commit after each chain",
+             2: "+ satisfied wait and fence", 3: "dQ loop: SS, TS, SS"}
+    res = {}
+    for ctas, n_iter in ((1, 32), (n_sm, 32), (n_sm, 2048)):
+        for mode in names:
+            o = (ctypes.c_longlong * ctas)()
+            assert plib.probe_mma_seq(mode, n_iter, ctas, o) == 0
+            assert plib.probe_mma_seq(mode, n_iter, ctas, o) == 0
+            res[(ctas, n_iter, mode)] = float(np.median(np.array(o[:])) / (n_iter * 24))
+    with capsys.disabled():
+        print(f"\n  loop                              1 SM   {n_sm} SMs  {n_sm} SMs x 2048 iterations")
+        for mode, name in names.items():
+            print(f"  {name:32s} {res[(1, 32, mode)]:6.1f} {res[(n_sm, 32, mode)]:8.1f} {res[(n_sm, 2048, mode)]:8.1f}")
+    assert res[(1, 32, 0)] <= 1.3 * 64
