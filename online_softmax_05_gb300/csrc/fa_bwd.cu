@@ -452,12 +452,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ compute (warps 0-7) + dK/dV epilogue
-        const int h = warp >> 2, wq = warp & 3;
-        const int key = kt * kBN + 32 * wq + lane;
+        // Warpgroup h takes query columns 64h .. 64h+63.  TMEM is read and written
+        // in the 16-lane shapes: for half hf of the warp's 32 lanes, register
+        // 4k + i of a 16x256b load holds key row 16 hf + t/4 (+8 for i >= 2) and
+        // query column 64h + 8k + 2 (t % 4) + (i % 2); register 2k + i of a
+        // 16x128b store goes to key row 16 hf + t/4 (+8 for i = 1), pair column
+        // 4k + t % 4.  So each thread needs the -LSE2 and -D values of only 16
+        // query columns, 4 distinct addresses per warp and load.
+        const int h = warp >> 2, wq = warp & 3, t4 = lane & 3;
+        const int key_base = kt * kBN + 32 * wq + (lane >> 2);  // + 16 hf + 8 i2
         const uint32_t lane_base = tmem + ((32u * wq) << 16);
         const float eff = p.sl2_eff, sl2 = p.sl2;
         const bool prescale = p.prescale != 0;
-        constexpr int NCH = C::kHalf / 32;  // 32-column chunks per thread
+        const uint64_t eff2 = f2(eff, eff);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int st = it % NQS;
@@ -469,45 +476,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             if (warp == 0 && lane == 0) FA_TRACE_EVENT(3, it);
             tc_fence_after();
-            const float4* lse4 = reinterpret_cast<const float4*>(smem + (sLse(st) - sbase));
-            const float4* dv4 = reinterpret_cast<const float4*>(smem + (sDv(st) - sbase));
-            // P^T for all of this thread's columns (S^T fully read before P^T is written over it)
-            uint32_t sr[C::kHalf];
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) tmem_ld32(lane_base + C::kS + h * C::kHalf + 32 * ch, sr + 32 * ch);
+            // this thread's 16 query columns: 64h + 8k + 2 t4 + {0, 1}
+            const float2* lse2v = reinterpret_cast<const float2*>(smem + (sLse(st) - sbase)) + 32 * h + t4;
+            const float2* dv2v = reinterpret_cast<const float2*>(smem + (sDv(st) - sbase)) + 32 * h + t4;
+            uint32_t sr[64];
+            tmem_ld_16x256b_x8(lane_base + C::kS + 64 * h, sr);
+            tmem_ld_16x256b_x8(lane_base + (16u << 16) + C::kS + 64 * h, sr + 32);
             tmem_ld_wait();
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) reg_fence32(sr + 32 * ch);
+            reg_fence32(sr);
+            reg_fence32(sr + 32);
             float* pf = reinterpret_cast<float*>(sr);
             if (prescale) {
 #pragma unroll
-                for (int e = 0; e < C::kHalf; ++e) pf[e] *= sl2;
+                for (int e = 0; e < 64; ++e) pf[e] *= sl2;
             }
-            // P^T = exp2(S^T c - LSE2): one packed FMA per pair (the smem vector holds -LSE2)
-            const uint64_t eff2 = f2(eff, eff);
+            // P^T = exp2(S^T c - LSE2): one packed FMA per pair of columns
 #pragma unroll
-            for (int e4 = 0; e4 < C::kHalf / 4; ++e4) {
-                const float4 l4 = lse4[(h * C::kHalf) / 4 + e4];
-                float x0, x1, x2, x3;
-                f2_split(fma2(f2(pf[4 * e4 + 0], pf[4 * e4 + 1]), eff2, f2(l4.x, l4.y)), x0, x1);
-                f2_split(fma2(f2(pf[4 * e4 + 2], pf[4 * e4 + 3]), eff2, f2(l4.z, l4.w)), x2, x3);
-                pf[4 * e4 + 0] = ex2_approx(x0);
-                pf[4 * e4 + 1] = ex2_approx(x1);
-                pf[4 * e4 + 2] = ex2_approx(x2);
-                pf[4 * e4 + 3] = ex2_approx(x3);
+            for (int k = 0; k < 8; ++k) {
+                const float2 l2 = lse2v[4 * k];
+                const uint64_t nl = f2(l2.x, l2.y);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {  // r = 2 hf + i2
+                    const int e = 32 * (r >> 1) + 4 * k + 2 * (r & 1);
+                    float x0, x1;
+                    f2_split(fma2(f2(pf[e], pf[e + 1]), eff2, nl), x0, x1);
+                    pf[e] = ex2_approx(x0);
+                    pf[e + 1] = ex2_approx(x1);
+                }
             }
             if (masked) {
 #pragma unroll
-                for (int e = 0; e < C::kHalf; ++e)
-                    if (!bwd_elem_visible(T, CAUSAL, q0 + h * C::kHalf + e, key)) pf[e] = 0.f;
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int e = 32 * (r >> 1) + 4 * k + 2 * (r & 1);
+                        const int key = key_base + 16 * (r >> 1) + 8 * (r & 1);
+                        const int q = q0 + 64 * h + 8 * k + 2 * t4;
+                        if (!bwd_elem_visible(T, CAUSAL, q, key)) pf[e] = 0.f;
+                        if (!bwd_elem_visible(T, CAUSAL, q + 1, key)) pf[e + 1] = 0.f;
+                    }
             }
-            {
-                uint32_t pk[C::kHalf / 2];
 #pragma unroll
-                for (int e = 0; e < C::kHalf / 2; ++e) pk[e] = pack_bf16x2(pf[2 * e], pf[2 * e + 1]);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < C::kHalf / 32; ++c)
-                    tmem_st16(lane_base + C::kP + h * (C::kHalf / 2) + 16 * c, pk + 16 * c);
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int i2 = 0; i2 < 2; ++i2) {
+                        const int e = 32 * hf + 4 * k + 2 * i2;
+                        pk[2 * k + i2] = pack_bf16x2(pf[e], pf[e + 1]);
+                    }
+                tmem_st_16x128b_x8(lane_base + ((16u * hf) << 16) + C::kP + 32 * h, pk);
             }
             // dV(it) needs only P^T: release it before dP^T is even ready
             tmem_st_wait();
@@ -521,34 +540,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             if (warp == 0 && lane == 0) FA_TRACE_EVENT(5, it);
             tc_fence_after();
-            uint32_t dr[C::kHalf];
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) tmem_ld32(lane_base + C::kDP + h * C::kHalf + 32 * ch, dr + 32 * ch);
+            uint32_t dr[64];
+            tmem_ld_16x256b_x8(lane_base + C::kDP + 64 * h, dr);
+            tmem_ld_16x256b_x8(lane_base + (16u << 16) + C::kDP + 64 * h, dr + 32);
             tmem_ld_wait();
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) reg_fence32(dr + 32 * ch);
+            reg_fence32(dr);
+            reg_fence32(dr + 32);
             // dS^T = P^T o (dP^T - D), bf16 pairs written over the dP^T columns this
             // warpgroup has just read (dP^T(it) completing implies dK(it-1), the
             // previous reader of those columns, completed: it was issued before)
+            uint32_t dsw[32];
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-                const int c0 = h * C::kHalf + 32 * ch;
-                uint32_t pk[16];
+            for (int k = 0; k < 8; ++k) {
+                const float2 d2 = dv2v[4 * k];
+                const uint64_t nd = f2(d2.x, d2.y);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const float4 da = dv4[(c0 + 8 * g) / 4], db = dv4[(c0 + 8 * g) / 4 + 1];
-                    const uint64_t nd[4] = {f2(da.x, da.y), f2(da.z, da.w), f2(db.x, db.y), f2(db.z, db.w)};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 32 * ch + 8 * g + 2 * e;
-                        const uint64_t t2 = add2(f2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), nd[e]);
-                        float d0, d1;
-                        f2_split(mul2(f2(pf[c], pf[c + 1]), t2), d0, d1);
-                        pk[4 * g + e] = pack_bf16x2(d0, d1);
-                    }
+                for (int r = 0; r < 4; ++r) {
+                    const int e = 32 * (r >> 1) + 4 * k + 2 * (r & 1);
+                    const uint64_t t2 = add2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd);
+                    float d0, d1;
+                    f2_split(mul2(f2(pf[e], pf[e + 1]), t2), d0, d1);
+                    dsw[16 * (r >> 1) + 2 * k + (r & 1)] = pack_bf16x2(d0, d1);
                 }
-                tmem_st16(lane_base + C::kDS + h * (C::kHalf / 2) + 16 * ch, pk);
             }
+            tmem_st_16x128b_x8(lane_base + C::kDS + 32 * h, dsw);
+            tmem_st_16x128b_x8(lane_base + (16u << 16) + C::kDS + 32 * h, dsw + 16);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -558,6 +574,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // epilogue: warpgroup 0 stores dK * scale, warpgroup 1 stores dV
         if (ok && warp_wait(dkv_full, 0, ctl)) {
             tc_fence_after();
+            const int key = kt * kBN + 32 * wq + lane;  // 32x32b shape: this thread's own lane
             const uint32_t col = h ? C::kDV : C::kDK;
             const float mul = h ? 1.f : p.scale;
             __nv_bfloat16* out = h ? p.dv : p.dk;

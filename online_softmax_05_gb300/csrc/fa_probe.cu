@@ -330,6 +330,59 @@ __global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_i
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// Lane/column layout of tcgen05.ld.16x256b.x8 and tcgen05.st.16x128b.x8.
+// Every TMEM cell (lane l, column c) of columns 0..63 is first written with
+// (l << 16) | c through 32x32b stores; each warp then loads its lanes
+// 32w .. 32w+15 and 32w+16 .. 32w+31 with the 16x256b shape and records the
+// 2 x 32 registers of each thread in ld_out[w][t][64].  Then each thread
+// stores 16 registers (w << 24) | (t << 16) | j with the 16x128b shape at
+// lanes 32w .. 32w+15, columns 128 .. 159, and the cells are read back with
+// 32x32b loads into st_out[lane][32].
+__global__ void __launch_bounds__(128, 1) probe_tmem_layout_kernel(uint32_t* ld_out, uint32_t* st_out) {
+    __shared__ uint32_t tslot;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tslot), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    const uint32_t lane_base = tmem + ((32u * warp) << 16);
+    const uint32_t l = 32u * warp + lane;
+    uint32_t v[32];
+    for (int half = 0; half < 2; ++half) {
+        for (int c = 0; c < 32; ++c) v[c] = (l << 16) | (32u * half + c);
+        tmem_st32(lane_base + 32 * half, v);
+    }
+    tmem_st_wait();
+    for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld_16x256b_x8(lane_base + ((16u * half) << 16), r);
+        tmem_ld_wait();
+        reg_fence32(r);
+        for (int j = 0; j < 32; ++j) ld_out[(warp * 32 + lane) * 64 + 32 * half + j] = r[j];
+    }
+    uint32_t w16[16];
+    for (int j = 0; j < 16; ++j) w16[j] = (uint32_t(warp) << 24) | (uint32_t(lane) << 16) | uint32_t(j);
+    for (int c = 0; c < 32; ++c) v[c] = 0xffffffffu;
+    tmem_st32(lane_base + 128, v);
+    tmem_st_wait();
+    tmem_st_16x128b_x8(lane_base + 128, w16);
+    tmem_st_wait();
+    {
+        uint32_t r[32];
+        tmem_ld32(lane_base + 128, r);
+        tmem_ld_wait();
+        reg_fence32(r);
+        for (int c = 0; c < 32; ++c) st_out[l * 32 + c] = r[c];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // Throughput of exp2: mode 0 = ex2.approx (MUFU), mode 1 = polynomial on
 // the FMA/ALU pipes (round-to-nearest by the 1.5*2^23 add, degree-3
 // least-squares fit of 2^f on [-1/2, 1/2], integer add into the exponent).
@@ -427,6 +480,19 @@ int probe_mma_seq(int mode, int n_iter, int ctas, long long* out_host) {
     cudaFree(out);
     if (e != cudaSuccess) return -5;
     return h ? -7 : 0;
+}
+
+int probe_tmem_layout(uint32_t* ld_host, uint32_t* st_host) {
+    uint32_t *ld = nullptr, *st = nullptr;
+    if (cudaMalloc(&ld, 128 * 64 * 4) != cudaSuccess) return -5;
+    if (cudaMalloc(&st, 128 * 32 * 4) != cudaSuccess) return -5;
+    fa::probe_tmem_layout_kernel<<<1, 128>>>(ld, st);
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaMemcpy(ld_host, ld, 128 * 64 * 4, cudaMemcpyDeviceToHost);
+    cudaMemcpy(st_host, st, 128 * 32 * 4, cudaMemcpyDeviceToHost);
+    cudaFree(ld);
+    cudaFree(st);
+    return e == cudaSuccess ? 0 : -5;
 }
 
 int probe_mma(int a_mode, int b_mode, int N, int K, const void* A, const void* B, float* out) {

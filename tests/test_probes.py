@@ -121,3 +121,32 @@ def test_mma_sequence_report(plib, capsys):
         for mode, name in names.items():
             print(f"  {name:32s} {res[(1, 32, mode)]:6.1f} {res[(n_sm, 32, mode)]:8.1f} {res[(n_sm, 2048, mode)]:8.1f}")
     assert res[(1, 32, 0)] <= 1.3 * 64
+
+
+@pytest.mark.gpu
+def test_tmem_16x256b_load_and_16x128b_store_layout(plib):
+    """tcgen05.ld.16x256b.x8: thread t, register j = 4k + i holds lane
+    t/4 (+8 for i >= 2), column 8k + 2 (t % 4) + (i % 2).
+    tcgen05.st.16x128b.x8: thread t, register j = 2k + i lands in lane
+    t/4 (+8 for i = 1), column 4k + t % 4."""
+    ld = (ctypes.c_uint32 * (128 * 64))()
+    st = (ctypes.c_uint32 * (128 * 32))()
+    plib.probe_tmem_layout.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)]
+    assert plib.probe_tmem_layout(ld, st) == 0
+    ld = np.array(ld, dtype=np.uint32).reshape(4, 32, 2, 32)
+    for w in range(4):
+        for t in range(32):
+            for half in range(2):
+                for j in range(32):
+                    k, i = divmod(j, 4)
+                    lane = 32 * w + 16 * half + t // 4 + (8 if i >= 2 else 0)
+                    col = 8 * k + 2 * (t % 4) + (i % 2)
+                    assert ld[w, t, half, j] == (lane << 16) | col, (w, t, half, j, hex(ld[w, t, half, j]))
+    st = np.array(st, dtype=np.uint32).reshape(128, 32)
+    for w in range(4):
+        for t in range(32):
+            for j in range(16):
+                k, i = divmod(j, 2)
+                lane = 32 * w + t // 4 + (8 if i == 1 else 0)
+                col = 4 * k + t % 4
+                assert st[lane, col] == (w << 24) | (t << 16) | j, (w, t, j, hex(st[lane, col]))
