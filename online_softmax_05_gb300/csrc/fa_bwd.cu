@@ -81,7 +81,6 @@ __device__ __forceinline__ uint8_t* smem_window(uint8_t* raw) {
 template <int D>
 struct DkvCfg {
     static constexpr int BM = bwd_bm(D);             // query rows per inner iteration
-    static constexpr int kHalf = BM / 2;             // query columns per compute warpgroup
     static constexpr int kAtomsD = D / 64;
     static constexpr int kKVBytes = 128 * D * 2;     // one K or V tile
     static constexpr int kQBytes = BM * D * 2;       // one Q or dO tile
@@ -127,8 +126,9 @@ struct DqCfg {
     static constexpr int kKOff = 2 * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-    // qdo_full, k_full[], k_empty[], v_full[], v_empty[], s_full[2], dp_full, ds_full, dq_full, epi, mma_done
-    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 5;
+    // qdo_full, qdo_empty, k_full[], k_empty[], v_full[], v_empty[], s_full[2], dp_full, ds_full, dq_full,
+    // dq_empty, mma_done
+    static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 5;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kPayload = kMiscOff + 16;
     static constexpr int kSlack = (kPayload + 1024 <= kSmemLimit) ? 1024 : 0;
@@ -148,6 +148,8 @@ struct DqCfg {
 struct BwdParams {
     const float* lse2;   // [B*Hq][T_pad] -LSE * log2(e)
     const float* dvec;   // [B*Hq][T_pad] -D
+    __nv_bfloat16* dq;    // dQ kernel: output, stored row by row
+    int n_items;          // dQ kernel: (query tile, query head) work items
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     int T, T_pad, n_kt;   // n_kt = 128-row tiles (key tiles = query tiles)
@@ -609,11 +611,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ kernel
+// Work item w of a CTA (persistent grid, one CTA per SM): the items are
+// (query tile, query head), heaviest query tiles first across all heads (more
+// key tiles under causal masking); CTA b takes items b, 2G-1-b, 2G+b, ...
+// (snake order), which balances the heavy and light tiles.  Measured against
+// a head-major order (better L2 reuse of K and V), the balance wins.
+__device__ __forceinline__ int dq_item_of(int k, int n_items) {
+    const int G = gridDim.x;
+    const int w = k * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
+    return w < n_items ? w : -1;
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const __grid_constant__ CUtensorMap tm_dq, BwdParams p) {
+                     BwdParams p) {
     using C = DqCfg<D>;
     constexpr int NKS = C::kKStages, NVS = C::kVStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -629,17 +642,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto sK = [&](int st) { return sbase + C::kKOff + st * C::kTileBytes; };
     auto sV = [&](int st) { return sbase + C::kVOff + st * C::kTileBytes; };
     const uint32_t bars = sbase + C::kBarOff;
-    const uint32_t qdo_full = bars;
-    auto k_full = [&](int st) { return bars + 8u * (1 + st); };
-    auto k_empty = [&](int st) { return bars + 8u * (1 + NKS + st); };
-    auto v_full = [&](int st) { return bars + 8u * (1 + 2 * NKS + st); };
-    auto v_empty = [&](int st) { return bars + 8u * (1 + 2 * NKS + NVS + st); };
-    const uint32_t b0 = bars + 8u * (1 + 2 * NKS + 2 * NVS);
-    auto s_full = [&](int b) { return b0 + 8u * b; };  // S(j) in TMEM buffer j & 1
-    const uint32_t dp_full = b0 + 16;                   // dP(j) in TMEM
-    const uint32_t ds_full = b0 + 24;                   // dS(j) written over S(j), dP(j) read (8 warps)
-    const uint32_t dq_full = b0 + 32;                   // every dQ MMA done
-    const uint32_t epi = b0 + 40;                       // dQ tile staged in smem (8 warps)
+    const uint32_t qdo_full = bars, qdo_empty = bars + 8;
+    auto k_full = [&](int st) { return bars + 8u * (2 + st); };
+    auto k_empty = [&](int st) { return bars + 8u * (2 + NKS + st); };
+    auto v_full = [&](int st) { return bars + 8u * (2 + 2 * NKS + st); };
+    auto v_empty = [&](int st) { return bars + 8u * (2 + 2 * NKS + NVS + st); };
+    const uint32_t b0 = bars + 8u * (2 + 2 * NKS + 2 * NVS);
+    auto s_full = [&](int b) { return b0 + 8u * b; };  // S number g lands in buffer g & 1
+    const uint32_t dp_full = b0 + 16;                   // dP in TMEM
+    const uint32_t ds_full = b0 + 24;                   // dS written over S, dP read (8 warps)
+    const uint32_t dq_full = b0 + 32;                   // every dQ MMA of the item done
+    const uint32_t dq_empty = b0 + 40;                  // dQ read out of TMEM (8 warps)
     const uint32_t mma_done = b0 + 48;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
@@ -647,13 +660,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T;
-    // head-major order; within a head, heavy query tiles (more key tiles under causal masking) first
-    const int bh = blockIdx.x / p.n_kt, qt = p.n_kt - 1 - static_cast<int>(blockIdx.x % p.n_kt);
-    const int bh_kv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
-    const int n = fwd_num_kv_tiles(T, CAUSAL, qt);  // key tiles this query tile sees
+    struct Item {
+        int bh, qt, bh_kv, n;
+    };
+    auto item = [&](int w) {
+        Item it;
+        it.bh = w % p.BH;
+        it.qt = p.n_kt - 1 - w / p.BH;
+        it.bh_kv = (it.bh / p.Hq) * p.Hkv + (it.bh % p.Hq) / p.group;
+        it.n = fwd_num_kv_tiles(T, CAUSAL, it.qt);  // key tiles this query tile sees
+        return it;
+    };
 
     if (tid == 0) {
         mbar_init(qdo_full, 1);
+        mbar_init(qdo_empty, 1);
         for (int st = 0; st < NKS; ++st) {
             mbar_init(k_full(st), 1);
             mbar_init(k_empty(st), 1);
@@ -667,7 +688,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(dp_full, 1);
         mbar_init(ds_full, 8);
         mbar_init(dq_full, 1);
-        mbar_init(epi, 8);
+        mbar_init(dq_empty, 8);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -684,39 +705,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t k_armed = 0, v_armed = 0;
+            uint32_t kf = 0, vf = 0, qf = 0;  // fills issued (K ring, V ring, Q/dO pair)
             const uint64_t pol_kv = l2_policy_evict_last();   // K, V of a head serve all its query tiles
             const uint64_t pol_q = l2_policy_evict_first();
-            mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
-            for (int a = 0; a < C::kAtomsD; ++a) {
-                tma_load_3d_hint(sQ + a * 128 * 128, &tm_q, qdo_full, 64 * a, qt * 128, bh, pol_q);
-                tma_load_3d_hint(sdO + a * 128 * 128, &tm_do, qdo_full, 64 * a, qt * 128, bh, pol_q);
-            }
-            for (int j = 0; j < n; ++j) {
-                {
-                    const int st = j % NKS;
-                    if (!wait_bar(k_empty(st), ((j / NKS) & 1) ^ 1, ctl)) break;
-                    mbar_arrive_expect_tx(k_full(st), C::kTileBytes);
-                    ++k_armed;
-                    for (int a = 0; a < C::kAtomsD; ++a)
-                        tma_load_3d_hint(sK(st) + a * 128 * 128, &tm_k, k_full(st), 64 * a, j * kBN, bh_kv, pol_kv);
+            for (int k = 0;; ++k) {
+                const int w = dq_item_of(k, p.n_items);
+                if (w < 0) break;
+                const Item it = item(w);
+                if (!wait_bar(qdo_empty, (qf & 1) ^ 1, ctl)) break;
+                mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
+                ++qf;
+                for (int a = 0; a < C::kAtomsD; ++a) {
+                    tma_load_3d_hint(sQ + a * 128 * 128, &tm_q, qdo_full, 64 * a, it.qt * 128, it.bh, pol_q);
+                    tma_load_3d_hint(sdO + a * 128 * 128, &tm_do, qdo_full, 64 * a, it.qt * 128, it.bh, pol_q);
                 }
-                {
-                    const int st = j % NVS;
-                    if (!wait_bar(v_empty(st), ((j / NVS) & 1) ^ 1, ctl)) break;
-                    mbar_arrive_expect_tx(v_full(st), C::kTileBytes);
-                    ++v_armed;
-                    for (int a = 0; a < C::kAtomsD; ++a)
-                        tma_load_3d_hint(sV(st) + a * 128 * 128, &tm_v, v_full(st), 64 * a, j * kBN, bh_kv, pol_kv);
+                bool fail = false;
+                for (int j = 0; j < it.n; ++j) {
+                    {
+                        const int st = kf % NKS;
+                        if (!wait_bar(k_empty(st), ((kf / NKS) & 1) ^ 1, ctl)) {
+                            fail = true;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(k_full(st), C::kTileBytes);
+                        ++kf;
+                        for (int a = 0; a < C::kAtomsD; ++a)
+                            tma_load_3d_hint(sK(st) + a * 128 * 128, &tm_k, k_full(st), 64 * a, j * kBN, it.bh_kv,
+                                             pol_kv);
+                    }
+                    {
+                        const int st = vf % NVS;
+                        if (!wait_bar(v_empty(st), ((vf / NVS) & 1) ^ 1, ctl)) {
+                            fail = true;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(v_full(st), C::kTileBytes);
+                        ++vf;
+                        for (int a = 0; a < C::kAtomsD; ++a)
+                            tma_load_3d_hint(sV(st) + a * 128 * 128, &tm_v, v_full(st), 64 * a, j * kBN, it.bh_kv,
+                                             pol_kv);
+                    }
                 }
+                if (fail) break;
             }
+            // drain: copies still in flight must land before the CTA exits
             volatile int never = 0;
             Ctl drain{&never, 100000000ull};
-            wait_bar(qdo_full, 0, drain);
-            for (uint32_t f = k_armed > NKS ? k_armed - NKS : 0; f < k_armed; ++f)
-                wait_bar(k_full(f % NKS), (f / NKS) & 1, drain);
-            for (uint32_t f = v_armed > NVS ? v_armed - NVS : 0; f < v_armed; ++f)
-                wait_bar(v_full(f % NVS), (f / NVS) & 1, drain);
+            if (qf) wait_bar(qdo_full, (qf - 1) & 1, drain);
+            for (uint32_t f = kf > NKS ? kf - NKS : 0; f < kf; ++f) wait_bar(k_full(f % NKS), (f / NKS) & 1, drain);
+            for (uint32_t f = vf > NVS ? vf - NVS : 0; f < vf; ++f) wait_bar(v_full(f % NVS), (f / NVS) & 1, drain);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
@@ -725,17 +762,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const SDesc dK_km = sdesc_make(sK(0), 16, 1024), dV_km = sdesc_make(sV(0), 16, 1024);
             const SDesc dK_mn = sdesc_make(sK(0), 128 * 128, 1024);
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
-            // S = Q K^T: M = 128 queries, N = 128 keys, K = D (both K-major)
-            auto issue_s = [&](int ks, int b) {
+            uint32_t kc = 0, vc = 0, sc = 0, dsc = 0, qc = 0, item_no = 0;  // K, V, S, dS, Q/dO consumed so far
+            // S number g = Q K_j^T into buffer g & 1: M = 128 queries, N = 128 keys, K = D (both K-major)
+            auto issue_s = [&](uint32_t kidx, uint32_t g) -> bool {
+                const int ks = kidx % NKS;
+                if (!wait_bar<kCritSleep>(k_full(ks), (kidx / NKS) & 1, ctl)) return false;
+                tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const uint32_t off = ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4;
-                    mma_ss_d(tmem + C::kS(b), dQ_km, off, dK_km, ks * kTile16 + off, C::kIdescS, s > 0);
+                    mma_ss_d(tmem + C::kS(g & 1), dQ_km, off, dK_km, ks * kTile16 + off, C::kIdescS, s > 0);
                 }
-                mma_commit(s_full(b));
+                mma_commit(s_full(g & 1));
+                return true;
             };
             // dP = dO V^T
-            auto issue_dp = [&](int vs) {
+            auto issue_dp = [&](uint32_t vidx) -> bool {
+                const int vs = vidx % NVS;
+                if (!wait_bar<kCritSleep>(v_full(vs), (vidx / NVS) & 1, ctl)) return false;
+                tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const uint32_t off = ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4;
@@ -743,52 +788,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 mma_commit(dp_full);
                 mma_commit(v_empty(vs));
+                return true;
             };
-            // Per key tile j, in issue order:
+            // Per item: S(0), dP(0), S(1); then per key tile j, in issue order:
             //   dP(j+1)                    the compute warps have read dP(j)
             //   dQ += dS(j) K_j            dS from TMEM (over S(j)), K MN-major
             //   S(j+2)                     into the buffer of S(j) (dQ(j) was its last reader)
             // The compute warps turn S(j+1) and dP(j+1) into dS(j+1) while these run.
-            if (!wait_bar(qdo_full, 0, ctl)) goto mma_teardown;
-            if (!wait_bar(k_full(0), 0, ctl)) goto mma_teardown;
-            tc_fence_after();
-            issue_s(0, 0);
-            if (!wait_bar(v_full(0), 0, ctl)) goto mma_teardown;
-            tc_fence_after();
-            issue_dp(0);
-            if (n > 1) {
-                if (!wait_bar(k_full(1), 0, ctl)) goto mma_teardown;
+            for (int k = 0;; ++k) {
+                const int w = dq_item_of(k, p.n_items);
+                if (w < 0) break;
+                const Item it = item(w);
+                if (!wait_bar(qdo_full, qc & 1, ctl)) goto mma_teardown;
+                ++qc;
                 tc_fence_after();
-                issue_s(1, 1);
-            }
-            for (int j = 0; j < n; ++j) {
-                const int b = j & 1, ks = j % NKS;
-                FA_TRACE_EVENT(12, j);
-                if (!wait_bar<kCritSleep>(ds_full, j & 1, ctl)) goto mma_teardown;
-                FA_TRACE_EVENT(13, j);
-                tc_fence_after();
-                if (j + 1 < n) {
-                    const int vs = (j + 1) % NVS;
-                    if (!wait_bar<kCritSleep>(v_full(vs), ((j + 1) / NVS) & 1, ctl)) goto mma_teardown;
+                if (!issue_s(kc, sc)) goto mma_teardown;
+                if (!issue_dp(vc)) goto mma_teardown;
+                if (it.n > 1 && !issue_s(kc + 1, sc + 1)) goto mma_teardown;
+                for (int j = 0; j < it.n; ++j) {
+                    FA_TRACE_EVENT(12, j);
+                    if (!wait_bar<kCritSleep>(ds_full, dsc & 1, ctl)) goto mma_teardown;
+                    ++dsc;
+                    FA_TRACE_EVENT(13, j);
                     tc_fence_after();
-                    issue_dp(vs);
-                }
-                FA_TRACE_EVENT(18, j);
+                    if (j + 1 < it.n && !issue_dp(vc + j + 1)) goto mma_teardown;
+                    FA_TRACE_EVENT(18, j);
+                    if (j == it.n - 1) mma_commit(qdo_empty);  // every S and dP of the item is issued
+                    if (j == 0) {
+                        // the previous item's dQ must have left TMEM
+                        if (!wait_bar<kCritSleep>(dq_empty, (item_no & 1) ^ 1, ctl)) goto mma_teardown;
+                        tc_fence_after();
+                    }
+                    const int ks = (kc + j) % NKS, b = (sc + j) & 1;
 #pragma unroll
-                for (int s = 0; s < kBN / 16; ++s)
-                    mma_ts_d(tmem + C::kDQ, tmem + C::kS(b) + C::kDSCol + s * 8, dK_mn, ks * kTile16 + s * (2048 >> 4),
-                             C::kIdescDQ, (j > 0 || s > 0) ? 1u : 0u);
-                mma_commit(k_empty(ks));
-                FA_TRACE_EVENT(19, j);
-                if (j + 2 < n) {
-                    const int ks2 = (j + 2) % NKS;
-                    if (!wait_bar<kCritSleep>(k_full(ks2), ((j + 2) / NKS) & 1, ctl)) goto mma_teardown;
-                    tc_fence_after();
-                    issue_s(ks2, b);
+                    for (int s = 0; s < kBN / 16; ++s)
+                        mma_ts_d(tmem + C::kDQ, tmem + C::kS(b) + C::kDSCol + s * 8, dK_mn,
+                                 ks * kTile16 + s * (2048 >> 4), C::kIdescDQ, (j > 0 || s > 0) ? 1u : 0u);
+                    mma_commit(k_empty(ks));
+                    FA_TRACE_EVENT(19, j);
+                    if (j + 2 < it.n && !issue_s(kc + j + 2, sc + j + 2)) goto mma_teardown;
+                    FA_TRACE_EVENT(14, j);
                 }
-                FA_TRACE_EVENT(14, j);
+                mma_commit(dq_full);
+                kc += it.n;
+                vc += it.n;
+                sc += it.n;
+                ++item_no;
             }
-            mma_commit(dq_full);
         mma_teardown:
             mma_commit(mma_done);
             volatile int never = 0;
@@ -800,113 +846,110 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // thread = query row (TMEM lane); warpgroup h takes key columns 64h .. 64h+63
         const int h = warp >> 2, wq = warp & 3;
         const int r = 32 * wq + lane;
-        const int q = qt * 128 + r;
         const uint32_t lane_base = tmem + ((32u * wq) << 16);
         const float eff = p.sl2_eff, sl2 = p.sl2;
         const bool prescale = p.prescale != 0;
-        // -LSE2 and -D of this row (0 on padded rows q >= T, which the mask zeroes anyway)
-        const float nlse = p.lse2[static_cast<size_t>(bh) * p.T_pad + q];
-        const float nd = p.dvec[static_cast<size_t>(bh) * p.T_pad + q];
-        const uint64_t nlse2 = f2(nlse, nlse), nd2 = f2(nd, nd), eff2 = f2(eff, eff);
-        bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            const int b = j & 1;
-            const bool masked = bwd_tile_class(T, CAUSAL, 128, qt, j) == kMasked;
-            if (!warp_wait<kCritSleep>(s_full(b), (j >> 1) & 1, ctl)) {
-                ok = false;
-                break;
-            }
-            if (warp == 0 && lane == 0) FA_TRACE_EVENT(15, j);
-            tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld32(lane_base + C::kS(b) + 64 * h, sr);
-            tmem_ld32(lane_base + C::kS(b) + 64 * h + 32, sr + 32);
-            tmem_ld_wait();
-            reg_fence32(sr);
-            reg_fence32(sr + 32);
-            float* pf = reinterpret_cast<float*>(sr);
-            if (prescale) {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) pf[e] *= sl2;
-            }
-            // P = exp2(S c - LSE2)
-#pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                float x0, x1;
-                f2_split(fma2(f2(pf[e], pf[e + 1]), eff2, nlse2), x0, x1);
-                pf[e] = ex2_approx(x0);
-                pf[e + 1] = ex2_approx(x1);
-            }
-            if (masked) {
-                const int key0 = j * kBN + 64 * h;
-#pragma unroll
-                for (int e = 0; e < 64; ++e)
-                    if (!bwd_elem_visible(T, CAUSAL, q, key0 + e)) pf[e] = 0.f;
-            }
-            if (!warp_wait<kCritSleep>(dp_full, j & 1, ctl)) {
-                ok = false;
-                break;
-            }
-            if (warp == 0 && lane == 0) FA_TRACE_EVENT(16, j);
-            tc_fence_after();
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                uint32_t dr[32];
-                tmem_ld32(lane_base + C::kDP + 64 * h + 32 * ch, dr);
+        const uint64_t eff2 = f2(eff, eff);
+        uint32_t sc = 0, vc = 0, item_no = 0;  // S and dP numbers, items done: as in the MMA warp
+        for (int k = 0;; ++k) {
+            const int w = dq_item_of(k, p.n_items);
+            if (w < 0) break;
+            const Item it = item(w);
+            const int q = it.qt * 128 + r;
+            // -LSE2 and -D of this row (0 on padded rows q >= T, which the mask zeroes anyway)
+            const float nlse = p.lse2[static_cast<size_t>(it.bh) * p.T_pad + q];
+            const float nd = p.dvec[static_cast<size_t>(it.bh) * p.T_pad + q];
+            const uint64_t nlse2 = f2(nlse, nlse), nd2 = f2(nd, nd);
+            for (int j = 0; j < it.n; ++j) {
+                const uint32_t g = sc + j, b = g & 1;
+                const bool masked = bwd_tile_class(T, CAUSAL, 128, it.qt, j) == kMasked;
+                if (!warp_wait<kCritSleep>(s_full(b), (g >> 1) & 1, ctl)) goto compute_done;
+                if (warp == 0 && lane == 0) FA_TRACE_EVENT(15, j);
+                tc_fence_after();
+                uint32_t sr[64];
+                tmem_ld32(lane_base + C::kS(b) + 64 * h, sr);
+                tmem_ld32(lane_base + C::kS(b) + 64 * h + 32, sr + 32);
                 tmem_ld_wait();
-                reg_fence32(dr);
-                // dS = P o (dP - D), bf16 pairs over this warpgroup's S columns
-                uint32_t pk[16];
+                reg_fence32(sr);
+                reg_fence32(sr + 32);
+                float* pf = reinterpret_cast<float*>(sr);
+                if (prescale) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const uint64_t t2 = add2(f2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2);
-                    float d0, d1;
-                    f2_split(mul2(f2(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]), t2), d0, d1);
-                    pk[e] = pack_bf16x2(d0, d1);
+                    for (int e = 0; e < 64; ++e) pf[e] *= sl2;
                 }
-                tmem_st16(lane_base + C::kS(b) + C::kDSCol + 32 * h + 16 * ch, pk);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ds_full);
-            if (warp == 0 && lane == 0) FA_TRACE_EVENT(17, j);
-        }
-        // epilogue: dQ * scale -> bf16 into the Q tile's smem (every S MMA that
-        // read Q completed before dq_full), then one TMA store clipped at T
-        if (ok && warp_wait(dq_full, 0, ctl)) {
-            tc_fence_after();
-            constexpr int kCols = D / 2;  // d columns per warpgroup
+                // P = exp2(S c - LSE2)
 #pragma unroll
-            for (int c = 0; c < kCols / 32; ++c) {
-                const int col0 = h * kCols + 32 * c;
-                uint32_t v[32];
-                tmem_ld32(lane_base + C::kDQ + col0, v);
+                for (int e = 0; e < 64; e += 2) {
+                    float x0, x1;
+                    f2_split(fma2(f2(pf[e], pf[e + 1]), eff2, nlse2), x0, x1);
+                    pf[e] = ex2_approx(x0);
+                    pf[e + 1] = ex2_approx(x1);
+                }
+                if (masked) {
+                    const int key0 = j * kBN + 64 * h;
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (!bwd_elem_visible(T, CAUSAL, q, key0 + e)) pf[e] = 0.f;
+                }
+                if (!warp_wait<kCritSleep>(dp_full, (vc + j) & 1, ctl)) goto compute_done;
+                if (warp == 0 && lane == 0) FA_TRACE_EVENT(16, j);
+                tc_fence_after();
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t dr[32];
+                    tmem_ld32(lane_base + C::kDP + 64 * h + 32 * ch, dr);
+                    tmem_ld_wait();
+                    reg_fence32(dr);
+                    // dS = P o (dP - D), bf16 pairs over this warpgroup's S columns
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint64_t t2 = add2(f2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2);
+                        float d0, d1;
+                        f2_split(mul2(f2(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]), t2), d0, d1);
+                        pk[e] = pack_bf16x2(d0, d1);
+                    }
+                    tmem_st16(lane_base + C::kS(b) + C::kDSCol + 32 * h + 16 * ch, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ds_full);
+                if (warp == 0 && lane == 0) FA_TRACE_EVENT(17, j);
+            }
+            sc += it.n;
+            vc += it.n;
+            // epilogue: dQ * scale -> bf16, stored row by row (d columns of this warpgroup);
+            // TMEM is handed back as soon as the values are in registers
+            {
+                if (!warp_wait(dq_full, item_no & 1, ctl)) goto compute_done;
+                ++item_no;
+                tc_fence_after();
+                constexpr int kCols = D / 2;  // d columns per warpgroup
+                uint32_t v[kCols];
+#pragma unroll
+                for (int c = 0; c < kCols / 32; ++c) tmem_ld32(lane_base + C::kDQ + h * kCols + 32 * c, v + 32 * c);
                 tmem_ld_wait();
-                reg_fence32(v);
-                const uint32_t atom = sQ + (col0 >> 6) * (128 * 128);
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const uint32_t chunk = ((col0 & 63) >> 3) + q4;
-                    uint32_t w4[4];
+                for (int c = 0; c < kCols / 32; ++c) reg_fence32(v + 32 * c);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dq_empty);
+                if (q < T) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.dq + (static_cast<size_t>(it.bh) * T + q) * D + h * kCols);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w4[e] = pack_bf16x2(__uint_as_float(v[8 * q4 + 2 * e]) * p.scale,
-                                            __uint_as_float(v[8 * q4 + 2 * e + 1]) * p.scale);
-                    st_shared_v4(atom + sw128_off(r, chunk), w4[0], w4[1], w4[2], w4[3]);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(epi);
-            if (warp == 0 && lane == 0) {
-                if (wait_bar(epi, 0, ctl)) {
-                    for (int a = 0; a < C::kAtomsD; ++a) tma_store_3d(&tm_dq, sQ + a * 128 * 128, 64 * a, qt * 128, bh);
-                    bulk_commit();
-                    bulk_wait0();
+                    for (int g = 0; g < kCols / 8; ++g) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]) * p.scale, __uint_as_float(v[8 * g + 1]) * p.scale);
+                        o.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]) * p.scale, __uint_as_float(v[8 * g + 3]) * p.scale);
+                        o.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]) * p.scale, __uint_as_float(v[8 * g + 5]) * p.scale);
+                        o.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]) * p.scale, __uint_as_float(v[8 * g + 7]) * p.scale);
+                        dst[g] = o;
+                    }
                 }
             }
         }
+    compute_done:;
     }
 
     tc_fence_before();
@@ -929,7 +972,7 @@ bool set_smem_once(K kern, int bytes, bool& done) {
 
 template <int D, bool CAUSAL>
 int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                  const CUtensorMap& tdq, BwdParams p, int BHq, int BHkv, cudaStream_t st, const DebugKnobs& dbg) {
+                  BwdParams p, int BHq, int BHkv, cudaStream_t st, const DebugKnobs& dbg, int num_sms) {
     static bool attr_a = false, attr_b = false;
     auto ka = fa_bwd_dkdv_kernel<D, CAUSAL>;
     auto kb = fa_bwd_dq_kernel<D, CAUSAL>;
@@ -941,7 +984,9 @@ int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     if (cudaGetLastError() != cudaSuccess) return -5;
     if (dbg.ev[3]) cudaEventRecord(dbg.ev[3], st);
     p.BH = BHq;
-    kb<<<p.n_kt * BHq, kBwdThreads, DqCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
+    p.n_items = p.n_kt * BHq;
+    const int grid_b = p.n_items < num_sms ? p.n_items : num_sms;  // persistent: one CTA per SM
+    kb<<<grid_b, kBwdThreads, DqCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, p);
     if (cudaGetLastError() != cudaSuccess) return -5;
     if (dbg.ev[4]) cudaEventRecord(dbg.ev[4], st);
     return 0;
@@ -957,10 +1002,9 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     const size_t bytes_vec = (static_cast<size_t>(BH) * T_pad * 4 + 255) / 256 * 256;
     float* dvec = static_cast<float*>(ws);
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_vec);
-    CUtensorMap tq, tk, tv, tdo, tdq;
+    CUtensorMap tq, tk, tv, tdo;
     if (!make_tmap_bhtd(&tq, q, BH, T, D, 128) || !make_tmap_bhtd(&tk, k, BHkv, T, D, 128) ||
-        !make_tmap_bhtd(&tv, v, BHkv, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, 128) ||
-        !make_tmap_bhtd(&tdq, dq, BH, T, D, 128))
+        !make_tmap_bhtd(&tv, v, BHkv, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, 128))
         return -5;
     const long long rows = static_cast<long long>(BH) * T_pad;
     const long long blocks = (rows * (D / 8) + 255) / 256;
@@ -977,6 +1021,8 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     BwdParams p;
     p.lse2 = lse2;
     p.dvec = dvec;
+    p.dq = static_cast<__nv_bfloat16*>(dq);
+    p.n_items = 0;
     p.dk = static_cast<__nv_bfloat16*>(dk);
     p.dv = static_cast<__nv_bfloat16*>(dv);
     p.T = T;
@@ -992,10 +1038,10 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     p.sl2_eff = p.prescale ? 1.f : p.sl2;
     p.timeout_ns = dbg.timeout_ns;
     if (D == 64)
-        return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdq, p, BH, BHkv, stream, dbg)
-                      : launch_main_t<64, false>(tq, tk, tv, tdo, tdq, p, BH, BHkv, stream, dbg);
-    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdq, p, BH, BHkv, stream, dbg)
-                  : launch_main_t<128, false>(tq, tk, tv, tdo, tdq, p, BH, BHkv, stream, dbg);
+        return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, p, BH, BHkv, stream, dbg, num_sms)
+                      : launch_main_t<64, false>(tq, tk, tv, tdo, p, BH, BHkv, stream, dbg, num_sms);
+    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, p, BH, BHkv, stream, dbg, num_sms)
+                  : launch_main_t<128, false>(tq, tk, tv, tdo, p, BH, BHkv, stream, dbg, num_sms);
 }
 
 }  // namespace
