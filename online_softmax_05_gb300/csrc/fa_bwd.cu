@@ -615,7 +615,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // (query tile, query head), heaviest query tiles first across all heads (more
 // key tiles under causal masking); CTA b takes items b, 2G-1-b, 2G+b, ...
 // (snake order), which balances the heavy and light tiles.  Measured against
-// a head-major order (better L2 reuse of K and V), the balance wins.
+// a head-major order and against groups of 4, 8 or 16 heads (better L2 reuse
+// of K and V), the balance wins.
 __device__ __forceinline__ int dq_item_of(int k, int n_items) {
     const int G = gridDim.x;
     const int w = k * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));

@@ -513,22 +513,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 // O already holds PV(j-1) (S(j) was committed after it); rescale it
                 // before PV(j) is issued, only when some row's reference max moved.
                 if (__any_sync(0xffffffffu, need)) {
+                    // all D columns in flight at once (the S registers are free again):
+                    // one load latency instead of one per 32-column chunk
+                    uint32_t* orr = sr;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t orr[32];
-                        tmem_ld32(tO + 32 * c, orr);
-                        tmem_ld_wait();
-                        reg_fence32(orr);
-                        const uint64_t a2 = f2(alpha, alpha);
+                    for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, orr + 32 * c);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float o0, o1;
-                            f2_split(mul2(f2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2), o0, o1);
-                            orr[e] = __float_as_uint(o0);
-                            orr[e + 1] = __float_as_uint(o1);
-                        }
-                        tmem_st32(tO + 32 * c, orr);
+                    for (int c = 0; c < D / 32; ++c) reg_fence32(orr + 32 * c);
+                    const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+                    for (int e = 0; e < D; e += 2) {
+                        float o0, o1;
+                        f2_split(mul2(f2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2), o0, o1);
+                        orr[e] = __float_as_uint(o0);
+                        orr[e + 1] = __float_as_uint(o1);
                     }
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) tmem_st32(tO + 32 * c, orr + 32 * c);
                 }
                 tmem_st_wait();
                 tc_fence_before();
