@@ -524,31 +524,66 @@ def main():
                   (dkdv_ms, roofline("fa_bwd_dkdv_kernel", dkdv_tflops)),
                   (dq_ms, roofline("fa_bwd_dq_kernel", dq_tflops))], key=lambda x: -x[0])
 
-    # end to end through the public API with host buffers (pinned), copies timed
+    # End to end through the public API with host buffers (pinned), copies timed.
+    # Every step uploads its inputs (Q, K, V, dO) and downloads its results
+    # (O, LSE, dQ, dK, dV).  Uploads and downloads run on their own streams
+    # into and out of two sets of device buffers, so step k+1's upload and step
+    # k-1's download overlap step k's kernels, as a caller of the API would
+    # pipeline them.
     e2e = None
     if not args.no_e2e:
         hq, hk, hv, hdo = (t.to("cpu").pin_memory() for t in (q, k, v, do))
         ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(4))
         hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         n_e2e = max(3, min(K, 20))
+        bufs = [dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv)]
+        bufs.append({name: torch.empty_like(t) for name, t in bufs[0].items()})
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        h2d_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        d2h_done = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
-                dst.copy_(src, non_blocking=True)
-            fa.attention_forward(q, k, v, causal=causal, scale=scale, out=o, lse=lse, stream=stream)
-            fa.attention_backward(q, k, v, o, lse, do, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv,
-                                  stream=stream)
-            for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
-                dst.copy_(src, non_blocking=True)
+        def upload(bf):
+            with torch.cuda.stream(s_in):
+                for name, src in (("q", hq), ("k", hk), ("v", hv), ("do", hdo)):
+                    bf[name].copy_(src, non_blocking=True)
 
-        e2e_step()
+        def e2e_run(n):
+            upload(bufs[0])
+            h2d_done[0].record(s_in)
+            for st in range(n):
+                b = st % 2
+                bf = bufs[b]
+                stream.wait_event(h2d_done[b])
+                if st >= 2:
+                    stream.wait_event(d2h_done[b])  # step st-2's results have left these buffers
+                fa.attention_forward(bf["q"], bf["k"], bf["v"], causal=causal, scale=scale, out=bf["o"],
+                                     lse=bf["lse"], stream=stream)
+                fa.attention_backward(bf["q"], bf["k"], bf["v"], bf["o"], bf["lse"], bf["do"], causal=causal,
+                                      scale=scale, dq=bf["dq"], dk=bf["dk"], dv=bf["dv"], stream=stream)
+                comp_done[b].record(stream)
+                if st + 1 < n:
+                    nb = (st + 1) % 2
+                    if st >= 1:
+                        s_in.wait_event(comp_done[nb])  # step st-1's kernels are done with its inputs
+                    upload(bufs[nb])
+                    h2d_done[nb].record(s_in)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(comp_done[b])
+                    for dst, name in ((ho, "o"), (hlse, "lse"), (hdq, "dq"), (hdk, "dk"), (hdv, "dv")):
+                        dst.copy_(bf[name], non_blocking=True)
+                d2h_done[b].record(s_out)
+            stream.wait_event(d2h_done[(n - 1) % 2])
+
+        e2e_run(2)
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if dist is not None:
             dist.barrier()
         a.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
+        s_in.wait_event(a)
+        s_out.wait_event(a)
+        e2e_run(n_e2e)
         b.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = a.elapsed_time(b) / n_e2e
@@ -559,7 +594,8 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
         d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
         e2e = {"value": world * step_fl / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "copies": "upload and download streams, two device buffer sets, overlapped with the kernels"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
