@@ -3,7 +3,10 @@
 // tile; dV = P^T dO; dP = dO V^T; dS = P o (dP - D); dQ = dS K scale;
 // dK = dS^T Q scale).
 //
-// Three kernels on the caller's stream:
+// The backward is split as "Lab 06", "Stretch" describes: one kernel with key
+// tiles outer for dK and dV, one with query tiles outer for dQ, each
+// recomputing S and dP, so that no tile's contribution needs a reduction in
+// global memory.  Three kernels on the caller's stream:
 //   fa_bwd_pre   D_i = sum_d dO_id O_id (fp32) and LSE in log2 units, both
 //                stored negated and padded to a multiple of 128 rows.
 //   fa_bwd_dkdv  key tiles outer, query tiles inner ("Lab 06", section 4:
