@@ -75,7 +75,8 @@ struct FwdCfg {
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
     // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] epi[2] mma_done
-    static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1;
+    // ph_full[2]
+    static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1 + 2;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + tmem slot, abort flag, alignment slack
     // TMEM columns (512 allocated): S0, S1 (P aliases their first 64 columns), O0, O1
@@ -231,6 +232,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     auto o_full = [&](int t) { return bars + 8u * (8 + 2 * C::kStages + t); };
     auto epi_bar = [&](int t) { return bars + 8u * (10 + 2 * C::kStages + t); };
     const uint32_t mma_done = bars + 8u * (12 + 2 * C::kStages);
+    // ph_full(t): the first half of P (keys 0..63) and the O rescale are done
+    auto ph_full = [&](int t) { return bars + 8u * (13 + 2 * C::kStages + t); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
     const Ctl ctl{abort_flag, p.timeout_ns};
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(q_empty(t), 1);
             mbar_init(s_full(t), 1);
             mbar_init(p_full(t), 4);
+            mbar_init(ph_full(t), 4);
             mbar_init(o_full(t), 1);
             mbar_init(epi_bar(t), 4);
         }
@@ -342,10 +346,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     mma_ss_d(tmem + C::kS(t), dQ_km, qo + off, dKV_km, ko + off, C::kIdescS, s > 0);
                 }
             };
-            auto issue_pv = [&](int t, uint32_t slot, bool acc) {
+            // half h of O += P V: keys 64h .. 64h+63 (k-steps 4h .. 4h+3)
+            auto issue_pv_half = [&](int t, uint32_t slot, bool acc, int h) {
                 const uint32_t vo = slot * kTile16;
 #pragma unroll
-                for (int s = 0; s < kBN / 16; ++s)
+                for (int s = 4 * h; s < 4 * h + 4; ++s)
                     mma_ts_d(tmem + C::kO(t), tmem + C::kS(t) + s * 8, dKV_mn, vo + s * (2048 >> 4), C::kIdescPV,
                              (acc || s > 0) ? 1u : 0u);
             };
@@ -388,11 +393,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int t = 0; t < 2; ++t) {
                         const int n = t ? n1 : n0;
                         if (j >= n) continue;
+                        // the first half of P·V as soon as its half of P is in TMEM
+                        if (!wait_bar<kCritSleep>(ph_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
+                        tc_fence_after();
+                        issue_pv_half(t, vs, j > 0, 0);
                         if (!wait_bar<kCritSleep>(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
                         FA_FTRACE(0 + t, j);
                         ++p_cnt[t];
                         tc_fence_after();
-                        issue_pv(t, vs, j > 0);
+                        issue_pv_half(t, vs, true, 1);
                         if (j + 1 < n) {
                             if (!k_ready) {
                                 if (!wait_bar<kCritSleep>(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
@@ -490,11 +499,51 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     m_used = m_new;
                     l *= alpha;
                 }
-                // P = exp2(S * c - m): packed FMA for the argument, packed add for the row sum
+                // P = exp2(S * c - m) in two halves of 64 keys: packed FMA for the
+                // argument, packed add for the row sum.  The first half, together
+                // with the O rescale, is released to the MMA warp before the second
+                // half is computed, so the first half of P·V runs beside it.
                 const uint64_t eff2 = f2(eff, eff), neg2 = f2(-m_used, -m_used);
                 uint64_t lp2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 32; ++c) {
+                    float x0, x1;
+                    f2_split(fma2(f2(s[2 * c], s[2 * c + 1]), eff2, neg2), x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    lp2[c & 3] = add2(lp2[c & 3], f2(p0, p1));
+                    sr[c] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS, sr);
+                // O already holds PV(j-1) (S(j) was committed after it); rescale it
+                // before PV(j) starts, only when some row's reference max moved.  The
+                // first 64 S registers are free again: two 32-column chunks in flight.
+                if (__any_sync(0xffffffffu, need)) {
+                    uint32_t* orr = sr;
+                    const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+                    for (int c2 = 0; c2 < D / 64; ++c2) {
+                        tmem_ld32(tO + 64 * c2, orr);
+                        tmem_ld32(tO + 64 * c2 + 32, orr + 32);
+                        tmem_ld_wait();
+                        reg_fence32(orr);
+                        reg_fence32(orr + 32);
+#pragma unroll
+                        for (int e = 0; e < 64; e += 2) {
+                            float o0, o1;
+                            f2_split(mul2(f2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2), o0, o1);
+                            orr[e] = __float_as_uint(o0);
+                            orr[e + 1] = __float_as_uint(o1);
+                        }
+                        tmem_st32(tO + 64 * c2, orr);
+                        tmem_st32(tO + 64 * c2 + 32, orr + 32);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ph_full(t));
+#pragma unroll
+                for (int c = 32; c < 64; ++c) {
                     float x0, x1;
                     f2_split(fma2(f2(s[2 * c], s[2 * c + 1]), eff2, neg2), x0, x1);
                     const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -502,36 +551,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     sr[c] = pack_bf16x2(p0, p1);
                 }
                 {
-                    float a0, a1, b0, b1;
+                    float a0, a1;
                     f2_split(add2(add2(lp2[0], lp2[1]), add2(lp2[2], lp2[3])), a0, a1);
-                    (void)b0;
-                    (void)b1;
                     l += a0 + a1;
                 }
-                tmem_st32(tS, sr);
                 tmem_st32(tS + 32, sr + 32);
-                // O already holds PV(j-1) (S(j) was committed after it); rescale it
-                // before PV(j) is issued, only when some row's reference max moved.
-                if (__any_sync(0xffffffffu, need)) {
-                    // all D columns in flight at once (the S registers are free again):
-                    // one load latency instead of one per 32-column chunk
-                    uint32_t* orr = sr;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, orr + 32 * c);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) reg_fence32(orr + 32 * c);
-                    const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll
-                    for (int e = 0; e < D; e += 2) {
-                        float o0, o1;
-                        f2_split(mul2(f2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2), o0, o1);
-                        orr[e] = __float_as_uint(o0);
-                        orr[e + 1] = __float_as_uint(o1);
-                    }
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) tmem_st32(tO + 32 * c, orr + 32 * c);
-                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
