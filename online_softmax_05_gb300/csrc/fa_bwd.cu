@@ -200,6 +200,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) 
     if ((threadIdx.x & 31) == 0) ok = wait_bar<kSleep>(bar, parity, c);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
+// Bounded wait taken by every lane of a converged warp; the result is the same
+// in all lanes.  The MMA warps wait this way: the issue loop then stays
+// warp-uniform and elect.sync picks the lane that issues, which keeps the
+// tensor pipe fed across waits and fences (a loop run by lane 0 alone leaves
+// a gap of about 60 cycles at each wait).
+template <bool kSleep = false>
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, Ctl c) {
+    const bool ok = mbar_try_wait(bar, parity) || wait_slow<kSleep>(bar, parity, c);
+    return __all_sync(0xffffffffu, ok);
+}
 
 
 // ---------------------------------------------------------------- preprocess
@@ -378,7 +388,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop; the elected lane issues and commits.
+        {
+            const bool leader = elect_one_sync();
             // Descriptors are built once; a stage / k-step is an offset in 16-byte units.
             const SDesc dK_km = sdesc_make(sK, 16, 1024), dV_km = sdesc_make(sV, 16, 1024);
             const SDesc dQ_km = sdesc_make(sQ(0), 16, 1024), dO_km = sdesc_make(sdO(0), 16, 1024);
@@ -390,18 +402,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t so = st * kQStage16;
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s)
-                    mma_ss_d(tmem + C::kS, dK_km, ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4, dQ_km,
+                    if (leader) mma_ss_d(tmem + C::kS, dK_km, ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4, dQ_km,
                              so + (((s >> 2) * (BM * 128) + (s & 3) * 32) >> 4), C::kIdescS, s > 0);
-                mma_commit(s_full);
+                if (leader) mma_commit(s_full);
             };
             // dP^T = V dO^T
             auto issue_dp = [&](int st) {
                 const uint32_t so = st * kDOStage16;
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s)
-                    mma_ss_d(tmem + C::kDP, dV_km, ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4, dO_km,
+                    if (leader) mma_ss_d(tmem + C::kDP, dV_km, ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4, dO_km,
                              so + (((s >> 2) * (BM * 128) + (s & 3) * 32) >> 4), C::kIdescS, s > 0);
-                mma_commit(dp_full);
+                if (leader) mma_commit(dp_full);
             };
             // Per query tile i, in issue order:
             //   dV += P^T(i) dO(i)         P^T from TMEM (over S^T(i)), dO MN-major
@@ -410,55 +422,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             //   dP^T(i+1)                  into the dP^T columns (dK(i) was the last reader)
             // The compute warps turn dP^T(i) into dS^T(i) while dV(i) and S^T(i+1)
             // run, and S^T(i+1) into P^T(i+1) while dK(i) and dP^T(i+1) run.
-            if (!wait_bar(kv_full, 0, ctl)) goto mma_teardown;
-            if (!wait_bar(q_full(0), 0, ctl)) goto mma_teardown;
+            if (!wait_all(kv_full, 0, ctl)) goto mma_teardown;
+            if (!wait_all(q_full(0), 0, ctl)) goto mma_teardown;
             tc_fence_after();
             issue_s(0);
-            if (!wait_bar(do_full(0), 0, ctl)) goto mma_teardown;
+            if (!wait_all(do_full(0), 0, ctl)) goto mma_teardown;
             tc_fence_after();
             issue_dp(0);
             for (int it = 0; it < n_it; ++it) {
                 const int qs = it % NQS, ds = it % NDS;
                 FA_TRACE_EVENT(0, it);
-                if (!wait_bar<kCritSleep>(p_full, it & 1, ctl)) goto mma_teardown;
+                if (!wait_all(p_full, it & 1, ctl)) goto mma_teardown;
                 FA_TRACE_EVENT(1, it);
                 tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < NKV; ++s)
-                    mma_ts_d(tmem + C::kDV, tmem + C::kP + s * 8, dO_mn, ds * kDOStage16 + s * (2048 >> 4),
+                    if (leader) mma_ts_d(tmem + C::kDV, tmem + C::kP + s * 8, dO_mn, ds * kDOStage16 + s * (2048 >> 4),
                              C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
-                mma_commit(do_empty(ds));
+                if (leader) mma_commit(do_empty(ds));
                 FA_TRACE_EVENT(7, it);
                 if (it + 1 < n_it) {
-                    if (!wait_bar<kCritSleep>(q_full((it + 1) % NQS), ((it + 1) / NQS) & 1, ctl))
+                    if (!wait_all(q_full((it + 1) % NQS), ((it + 1) / NQS) & 1, ctl))
                         goto mma_teardown;
                     tc_fence_after();
                     issue_s((it + 1) % NQS);
                 }
                 FA_TRACE_EVENT(2, it);
-                if (!wait_bar<kCritSleep>(ds_full, it & 1, ctl)) goto mma_teardown;
+                if (!wait_all(ds_full, it & 1, ctl)) goto mma_teardown;
                 FA_TRACE_EVENT(10, it);
                 tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < NKV; ++s)
-                    mma_ts_d(tmem + C::kDK, tmem + C::kDS + s * 8, dQ_mn, qs * kQStage16 + s * (2048 >> 4),
+                    if (leader) mma_ts_d(tmem + C::kDK, tmem + C::kDS + s * 8, dQ_mn, qs * kQStage16 + s * (2048 >> 4),
                              C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
-                mma_commit(q_empty(qs));
+                if (leader) mma_commit(q_empty(qs));
                 FA_TRACE_EVENT(11, it);
                 if (it + 1 < n_it) {
                     const int ds1 = (it + 1) % NDS;
-                    if (!wait_bar<kCritSleep>(do_full(ds1), ((it + 1) / NDS) & 1, ctl)) goto mma_teardown;
+                    if (!wait_all(do_full(ds1), ((it + 1) / NDS) & 1, ctl)) goto mma_teardown;
                     tc_fence_after();
                     issue_dp(ds1);
                     FA_TRACE_EVENT(8, it);
                 }
             }
-            mma_commit(dkv_full);
+            if (leader) mma_commit(dkv_full);
         mma_teardown:
-            mma_commit(mma_done);
-            volatile int never = 0;
-            Ctl drain{&never, 100000000ull};
-            wait_bar(mma_done, 0, drain);
+            if (leader) {
+                mma_commit(mma_done);
+                volatile int never = 0;
+                Ctl drain{&never, 100000000ull};
+                wait_bar(mma_done, 0, drain);
+            }
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------------------ compute (warps 0-7) + dK/dV epilogue
@@ -766,7 +781,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop; the elected lane issues and commits.
+        {
+            const bool leader = elect_one_sync();
             const SDesc dQ_km = sdesc_make(sQ, 16, 1024), dO_km = sdesc_make(sdO, 16, 1024);
             const SDesc dK_km = sdesc_make(sK(0), 16, 1024), dV_km = sdesc_make(sV(0), 16, 1024);
             const SDesc dK_mn = sdesc_make(sK(0), 128 * 128, 1024);
@@ -775,28 +792,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // S number g = Q K_j^T into buffer g & 1: M = 128 queries, N = 128 keys, K = D (both K-major)
             auto issue_s = [&](uint32_t kidx, uint32_t g) -> bool {
                 const int ks = kidx % NKS;
-                if (!wait_bar<kCritSleep>(k_full(ks), (kidx / NKS) & 1, ctl)) return false;
+                if (!wait_all(k_full(ks), (kidx / NKS) & 1, ctl)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const uint32_t off = ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4;
-                    mma_ss_d(tmem + C::kS(g & 1), dQ_km, off, dK_km, ks * kTile16 + off, C::kIdescS, s > 0);
+                    if (leader) mma_ss_d(tmem + C::kS(g & 1), dQ_km, off, dK_km, ks * kTile16 + off, C::kIdescS, s > 0);
                 }
-                mma_commit(s_full(g & 1));
+                if (leader) mma_commit(s_full(g & 1));
                 return true;
             };
             // dP = dO V^T
             auto issue_dp = [&](uint32_t vidx) -> bool {
                 const int vs = vidx % NVS;
-                if (!wait_bar<kCritSleep>(v_full(vs), (vidx / NVS) & 1, ctl)) return false;
+                if (!wait_all(v_full(vs), (vidx / NVS) & 1, ctl)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const uint32_t off = ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4;
-                    mma_ss_d(tmem + C::kDP, dO_km, off, dV_km, vs * kTile16 + off, C::kIdescS, s > 0);
+                    if (leader) mma_ss_d(tmem + C::kDP, dO_km, off, dV_km, vs * kTile16 + off, C::kIdescS, s > 0);
                 }
-                mma_commit(dp_full);
-                mma_commit(v_empty(vs));
+                if (leader) {
+                    mma_commit(dp_full);
+                    mma_commit(v_empty(vs));
+                }
                 return true;
             };
             // Per item: S(0), dP(0), S(1); then per key tile j, in issue order:
@@ -808,7 +827,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int w = dq_item_of(k, p.n_items);
                 if (w < 0) break;
                 const Item it = item(w);
-                if (!wait_bar(qdo_full, qc & 1, ctl)) goto mma_teardown;
+                if (!wait_all(qdo_full, qc & 1, ctl)) goto mma_teardown;
                 ++qc;
                 tc_fence_after();
                 if (!issue_s(kc, sc)) goto mma_teardown;
@@ -816,39 +835,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (it.n > 1 && !issue_s(kc + 1, sc + 1)) goto mma_teardown;
                 for (int j = 0; j < it.n; ++j) {
                     FA_TRACE_EVENT(12, j);
-                    if (!wait_bar<kCritSleep>(ds_full, dsc & 1, ctl)) goto mma_teardown;
+                    if (!wait_all(ds_full, dsc & 1, ctl)) goto mma_teardown;
                     ++dsc;
                     FA_TRACE_EVENT(13, j);
                     tc_fence_after();
                     if (j + 1 < it.n && !issue_dp(vc + j + 1)) goto mma_teardown;
                     FA_TRACE_EVENT(18, j);
-                    if (j == it.n - 1) mma_commit(qdo_empty);  // every S and dP of the item is issued
+                    if (j == it.n - 1 && leader) mma_commit(qdo_empty);  // every S and dP of the item is issued
                     if (j == 0) {
                         // the previous item's dQ must have left TMEM
-                        if (!wait_bar<kCritSleep>(dq_empty, (item_no & 1) ^ 1, ctl)) goto mma_teardown;
+                        if (!wait_all(dq_empty, (item_no & 1) ^ 1, ctl)) goto mma_teardown;
                         tc_fence_after();
                     }
                     const int ks = (kc + j) % NKS, b = (sc + j) & 1;
 #pragma unroll
                     for (int s = 0; s < kBN / 16; ++s)
-                        mma_ts_d(tmem + C::kDQ, tmem + C::kS(b) + C::kDSCol + s * 8, dK_mn,
+                        if (leader) mma_ts_d(tmem + C::kDQ, tmem + C::kS(b) + C::kDSCol + s * 8, dK_mn,
                                  ks * kTile16 + s * (2048 >> 4), C::kIdescDQ, (j > 0 || s > 0) ? 1u : 0u);
-                    mma_commit(k_empty(ks));
+                    if (leader) mma_commit(k_empty(ks));
                     FA_TRACE_EVENT(19, j);
                     if (j + 2 < it.n && !issue_s(kc + j + 2, sc + j + 2)) goto mma_teardown;
                     FA_TRACE_EVENT(14, j);
                 }
-                mma_commit(dq_full);
+                if (leader) mma_commit(dq_full);
                 kc += it.n;
                 vc += it.n;
                 sc += it.n;
                 ++item_no;
             }
         mma_teardown:
-            mma_commit(mma_done);
-            volatile int never = 0;
-            Ctl drain{&never, 100000000ull};
-            wait_bar(mma_done, 0, drain);
+            if (leader) {
+                mma_commit(mma_done);
+                volatile int never = 0;
+                Ctl drain{&never, 100000000ull};
+                wait_bar(mma_done, 0, drain);
+            }
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------------------ compute (warps 0-7) + dQ epilogue

@@ -141,6 +141,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c) 
     if ((threadIdx.x & 31) == 0) ok = wait_bar<kSleep>(bar, parity, c);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
+// Bounded wait taken by every lane of a converged warp; the result is the same
+// in all lanes.  The MMA warp waits this way: the issue loop then stays
+// warp-uniform and elect.sync picks the lane that issues, which keeps the
+// tensor pipe fed across waits and fences (a loop run by lane 0 alone leaves
+// a gap of about 60 cycles at each wait).
+template <bool kSleep = false>
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, Ctl c) {
+    const bool ok = mbar_try_wait(bar, parity) || wait_slow<kSleep>(bar, parity, c);
+    return __all_sync(0xffffffffu, ok);
+}
 
 // A work item: two 128-row query tiles that share every K/V tile they read.
 // Without grouped heads (or with an odd group) they are consecutive tiles of
@@ -331,7 +341,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop; the elected lane issues and commits.
+        {
+            const bool leader = elect_one_sync();
             uint32_t kv_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
             // Descriptors are built once; a tile / slot / k-step is an offset in 16-byte units.
             const SDesc dQ_km = sdesc_make(sQ[0], 16, 1024);
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const uint32_t off = ((s >> 2) * C::kAtomBytes + (s & 3) * 32) >> 4;
-                    mma_ss_d(tmem + C::kS(t), dQ_km, qo + off, dKV_km, ko + off, C::kIdescS, s > 0);
+                    if (leader) mma_ss_d(tmem + C::kS(t), dQ_km, qo + off, dKV_km, ko + off, C::kIdescS, s > 0);
                 }
             };
             // half h of O += P V: keys 64h .. 64h+63 (k-steps 4h .. 4h+3)
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const uint32_t vo = slot * kTile16;
 #pragma unroll
                 for (int s = 4 * h; s < 4 * h + 4; ++s)
-                    mma_ts_d(tmem + C::kO(t), tmem + C::kS(t) + s * 8, dKV_mn, vo + s * (2048 >> 4), C::kIdescPV,
+                    if (leader) mma_ts_d(tmem + C::kO(t), tmem + C::kS(t) + s * 8, dKV_mn, vo + s * (2048 >> 4), C::kIdescPV,
                              (acc || s > 0) ? 1u : 0u);
             };
             for (int k = 0;; ++k) {
@@ -363,28 +375,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const int n0 = fwd_num_kv_tiles(item.T, CAUSAL, item.tile[0]);
                 const int n1 = valid1 ? fwd_num_kv_tiles(item.T, CAUSAL, item.tile[1]) : 0;
                 const int nmax = n0 > n1 ? n0 : n1;
-                if (!wait_bar(q_full(0), q_cnt[0] & 1, ctl)) goto mma_done_label;
+                if (!wait_all(q_full(0), q_cnt[0] & 1, ctl)) goto mma_done_label;
                 ++q_cnt[0];
                 if (valid1) {
-                    if (!wait_bar(q_full(1), q_cnt[1] & 1, ctl)) goto mma_done_label;
+                    if (!wait_all(q_full(1), q_cnt[1] & 1, ctl)) goto mma_done_label;
                     ++q_cnt[1];
                 }
                 {
                     const uint32_t ks = kv_cnt % C::kStages;
-                    if (!wait_bar<kCritSleep>(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                    if (!wait_all(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                     ++kv_cnt;
                     tc_fence_after();
                     issue_s(0, ks);
-                    mma_commit(s_full(0));
+                    if (leader) mma_commit(s_full(0));
                     if (n1 > 0) {
                         issue_s(1, ks);
-                        mma_commit(s_full(1));
+                        if (leader) mma_commit(s_full(1));
                     }
-                    mma_commit(kv_empty(ks));
+                    if (leader) mma_commit(kv_empty(ks));
                 }
                 for (int j = 0; j < nmax; ++j) {
                     const uint32_t vs = kv_cnt % C::kStages;
-                    if (!wait_bar<kCritSleep>(kv_full(vs), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                    if (!wait_all(kv_full(vs), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                     ++kv_cnt;
                     tc_fence_after();
                     const bool has_next = j + 1 < nmax;
@@ -394,44 +406,47 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         const int n = t ? n1 : n0;
                         if (j >= n) continue;
                         // the first half of P·V as soon as its half of P is in TMEM
-                        if (!wait_bar<kCritSleep>(ph_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
+                        if (!wait_all(ph_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
                         tc_fence_after();
                         issue_pv_half(t, vs, j > 0, 0);
-                        if (!wait_bar<kCritSleep>(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
+                        if (!wait_all(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
                         FA_FTRACE(0 + t, j);
                         ++p_cnt[t];
                         tc_fence_after();
                         issue_pv_half(t, vs, true, 1);
                         if (j + 1 < n) {
                             if (!k_ready) {
-                                if (!wait_bar<kCritSleep>(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                                if (!wait_all(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                                 tc_fence_after();
                                 k_ready = true;
                             }
                             issue_s(t, ks);
-                            mma_commit(s_full(t));
+                            if (leader) mma_commit(s_full(t));
                         } else {
-                            mma_commit(o_full(t));
+                            if (leader) mma_commit(o_full(t));
                         }
                         FA_FTRACE(2 + t, j);
                     }
-                    mma_commit(kv_empty(vs));
+                    if (leader) mma_commit(kv_empty(vs));
                     if (has_next) {
                         if (!k_ready) {
-                            if (!wait_bar<kCritSleep>(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
+                            if (!wait_all(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                         }
-                        mma_commit(kv_empty(ks));
+                        if (leader) mma_commit(kv_empty(ks));
                         ++kv_cnt;
                     }
                 }
             }
         mma_done_label:
             // every MMA issued so far must finish before TMEM is released
-            mma_commit(mma_done);
-            Ctl drain{abort_flag, 100000000ull};
-            volatile int never = 0;
-            drain.abort = &never;
-            wait_bar(mma_done, 0, drain);
+            if (leader) {
+                mma_commit(mma_done);
+                Ctl drain{abort_flag, 100000000ull};
+                volatile int never = 0;
+                drain.abort = &never;
+                wait_bar(mma_done, 0, drain);
+            }
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------------------ softmax (tile t)

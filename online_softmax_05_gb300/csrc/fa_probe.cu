@@ -251,7 +251,16 @@ __global__ void __launch_bounds__(128, 1) probe_mma_chain_kernel(int N, int n, i
 //   mode 3  the dQ kernel's loop: SS (dP, columns 256), TS with A from
 //           columns 32.. of the S buffer (dQ, columns 384), SS (S, columns
 //           0 / 128 alternating), commits and waits as in mode 2
+// mode | 4: the same with the operands in shared memory filled with
+// pseudo-random bf16 values instead of 1.0.
+// SYNC (modes 2 and 3): 0 = wait, then fence; 1 = the wait alone; 2 = the
+// fence alone; 3 = the wait issued before the last two MMAs of the previous
+// chain, the fence after that chain.
+// WIDE: the whole warp runs the loop and elect.sync picks the issuing lane
+// (else lane 0 runs it alone).  RTOFF: the smem descriptors get an offset
+// known only at run time (always 0), like the kernels' ring stages.
 // Cycles from the first issue to the completion of the last MMA go to out[0].
+template <int SYNC, bool WIDE, bool RTOFF>
 __global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_iter, long long* out, int* err) {
     out += blockIdx.x;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -261,8 +270,22 @@ __global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_i
     const uint32_t bar = sB + 128 * 128 * 2;         // B: 128 rows x 128 (two atoms), 32 KB
     const uint32_t bar2 = bar + 8, bar3 = bar + 16;
     const uint32_t tslot = bar + 24;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    for (int i = tid; i < (2 * 128 * 128 * 2) / 4; i += 128) reinterpret_cast<uint32_t*>(smem)[i] = 0x3f803f80u;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool noisy = (mode & 4) != 0;
+    mode &= 3;
+    for (int i = tid; i < (2 * 128 * 128 * 2) / 4; i += 128) {
+        uint32_t w = 0x3f803f80u;  // 1.0 in both halves
+        if (noisy) {
+            // two bf16 of random sign, exponent 2^-8 .. 2^-1 and mantissa
+            // (an integer hash of the index: the values only have to toggle)
+            uint32_t h = uint32_t(i) * 0x9E3779B1u;
+            h ^= h >> 15;
+            h *= 0x85EBCA77u;
+            h ^= h >> 13;
+            w = (h & 0x807f807fu) | 0x3c003c00u | ((h >> 3) & 0x03800380u);
+        }
+        reinterpret_cast<uint32_t*>(smem)[i] = w;
+    }
     if (warp == 0) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -278,56 +301,75 @@ __global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_i
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tslot - sA));
-    if (tid == 0) {
-        mbar_arrive(bar3);  // a phase that has completed: waits on it return at once
+    if (tid == 0) mbar_arrive(bar3);  // a phase that has completed: waits on it return at once
+    __syncwarp();
+    if (warp == 0 && (WIDE || lane == 0)) {
+        const bool leader = WIDE ? elect_one_sync() : true;
         const uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
         const uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);
         const SDesc dA = sdesc_make(sA, 16, 1024), dB = sdesc_make(sB, 16, 1024);
         const SDesc dBmn = sdesc_make(sB, 128 * 128, 1024);
-        auto chain_ss = [&](uint32_t acc) {
+        bool early_ok = true;
+        auto chain_ss = [&](uint32_t acc, uint32_t so) {
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = ((s >> 2) * (128 * 128) + (s & 3) * 32) >> 4;
-                mma_ss_d(acc, dA, off, dB, off, id_kk, s > 0);
+                if (leader) mma_ss_d(acc, dA, off, dB, off + so, id_kk, s > 0);
+                if constexpr (SYNC == 3)
+                    if (s == 5 && mode >= 2) early_ok = mbar_try_wait(bar3, 0);
             }
         };
-        auto chain_ts = [&](uint32_t acc, uint32_t a_col) {
+        auto chain_ts = [&](uint32_t acc, uint32_t a_col, uint32_t so) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s) mma_ts_d(acc, a_col + s * 8, dBmn, s * (2048 >> 4), id_mn, 1u);
+            for (int s = 0; s < 8; ++s) {
+                if (leader) mma_ts_d(acc, a_col + s * 8, dBmn, s * (2048 >> 4) + so, id_mn, 1u);
+                if constexpr (SYNC == 3)
+                    if (s == 5) early_ok = mbar_try_wait(bar3, 0);
+            }
         };
         auto between = [&]() {
-            if (mode >= 1) mma_commit(bar2);
+            if (mode >= 1 && leader) mma_commit(bar2);
             if (mode >= 2) {
-                if (!mbar_try_wait(bar3, 0)) atomicExch(err, 3);
-                tc_fence_after();
+                if constexpr (SYNC == 0 || SYNC == 1)
+                    if (!mbar_try_wait(bar3, 0)) atomicExch(err, 3);
+                if constexpr (SYNC == 3)
+                    if (!early_ok) atomicExch(err, 3);
+                if constexpr (SYNC != 1) tc_fence_after();
             }
         };
         const long long t0 = clock64();
         for (int it = 0; it < n_iter; ++it) {
+            const uint32_t so = RTOFF ? (static_cast<uint32_t>(it) >> 20) << 10 : 0u;
             if (mode <= 2) {
-                chain_ss(tmem + 0);
+                chain_ss(tmem + 0, so);
                 between();
-                chain_ss(tmem + 128);
+                chain_ss(tmem + 128, so);
                 between();
-                chain_ss(tmem + 256);
+                chain_ss(tmem + 256, so);
                 between();
             } else {
-                chain_ss(tmem + 256);
+                chain_ss(tmem + 256, so);
                 between();
-                chain_ts(tmem + 384, tmem + (it & 1) * 128 + 32);
+                chain_ts(tmem + 384, tmem + (it & 1) * 128 + 32, so);
                 between();
-                chain_ss(tmem + (it & 1) * 128);
+                chain_ss(tmem + (it & 1) * 128, so);
                 between();
             }
         }
-        mma_commit(bar);
+        if (leader) mma_commit(bar);
         probe_wait(bar, 0, err);
-        out[0] = clock64() - t0;
+        if (lane == 0) out[0] = clock64() - t0;
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <int SYNC, bool WIDE, bool RTOFF>
+void launch_seq(int mode, int n_iter, long long* out, int* err, int ctas, int smem) {
+    cudaFuncSetAttribute(probe_mma_seq_kernel<SYNC, WIDE, RTOFF>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    probe_mma_seq_kernel<SYNC, WIDE, RTOFF><<<ctas, 128, smem>>>(mode, n_iter, out, err);
 }
 
 // Lane/column layout of tcgen05.ld.16x256b.x8 and tcgen05.st.16x128b.x8.
@@ -461,8 +503,9 @@ int probe_mma_chain(int N, int n, int chain, int kind, long long* out_host) {
 
 // ctas: number of CTAs (one per SM at this shared-memory size) running the
 // same sequence at once; out_host receives one count per CTA.
+// mode bits: 0-1 loop, 2 random operands, 3-4 SYNC, 5 WIDE, 6 RTOFF (see probe_mma_seq_kernel)
 int probe_mma_seq(int mode, int n_iter, int ctas, long long* out_host) {
-    if (mode < 0 || mode > 3 || n_iter < 1 || n_iter > 4096 || ctas < 1 || ctas > 1024) return -1;
+    if (mode < 0 || mode > 127 || n_iter < 1 || n_iter > 4096 || ctas < 1 || ctas > 1024) return -1;
     int* err = nullptr;
     long long* out = nullptr;
     if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) return -5;
@@ -470,8 +513,15 @@ int probe_mma_seq(int mode, int n_iter, int ctas, long long* out_host) {
     cudaMemset(err, 0, sizeof(int));
     // more than half of the SM's shared memory: at most one CTA per SM
     const int smem = 120 * 1024;
-    cudaFuncSetAttribute(fa::probe_mma_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    fa::probe_mma_seq_kernel<<<ctas, 128, smem>>>(mode, n_iter, out, err);
+    using Seq = void (*)(int, int, long long*, int*, int, int);
+    static const Seq kSeq[16] = {
+        fa::launch_seq<0, false, false>, fa::launch_seq<0, false, true>, fa::launch_seq<0, true, false>,
+        fa::launch_seq<0, true, true>,   fa::launch_seq<1, false, false>, fa::launch_seq<1, false, true>,
+        fa::launch_seq<1, true, false>,  fa::launch_seq<1, true, true>,   fa::launch_seq<2, false, false>,
+        fa::launch_seq<2, false, true>,  fa::launch_seq<2, true, false>,  fa::launch_seq<2, true, true>,
+        fa::launch_seq<3, false, false>, fa::launch_seq<3, false, true>,  fa::launch_seq<3, true, false>,
+        fa::launch_seq<3, true, true>};
+    kSeq[((mode >> 3) & 3) * 4 + ((mode >> 5) & 1) * 2 + ((mode >> 6) & 1)](mode & 7, n_iter, out, err, ctas, smem);
     cudaError_t e = cudaDeviceSynchronize();
     int h = 0;
     cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost);

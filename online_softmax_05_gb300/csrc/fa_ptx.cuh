@@ -256,6 +256,16 @@ __device__ __forceinline__ SDesc sdesc_make(uint32_t saddr, uint32_t lbo_bytes, 
     const uint64_t d = sdesc_sw128(saddr, lbo_bytes, sbo_bytes);
     return SDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
 }
+// One lane of the converged warp (the lowest active one) gets true.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok));
+    return ok != 0;
+}
 // mma_ss with descriptors a/b advanced by a_off16 / b_off16 (bytes >> 4).
 __device__ __forceinline__ void mma_ss_d(uint32_t d_tmem, SDesc a, uint32_t a_off16, SDesc b, uint32_t b_off16,
                                          uint32_t idesc, uint32_t accumulate) {

@@ -103,12 +103,25 @@ def test_mma_sequence_report(plib, capsys):
     """Cycles per 128x128x16 MMA for loops of three 8-instruction chains shaped
     like the attention kernels' (see probe_mma_seq_kernel): plain, with a
     commit after each chain, with commit + satisfied wait + fence, and the
-    dQ kernel's SS / TS / SS rotation; on one SM and on every SM at once."""
+    dQ kernel's SS / TS / SS rotation; on one SM and on every SM at once.
+    Then the first and the fourth with pseudo-random operands instead of 1.0
+    everywhere, and the wait / fence pair taken apart: the wait alone, the
+    fence alone, and the wait issued before the last two MMAs of the
+    previous chain; then the loop run by the whole warp with elect.sync
+    choosing the issuing lane, and descriptor offsets known only at run
+    time (as the kernels' ring stages are)."""
     import torch
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     plib.probe_mma_seq.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong)]
     names = {0: "3 accumulators, SS chains", 1: "+ commit after each chain",
-             2: "+ satisfied wait and fence", 3: "dQ loop: SS, TS, SS"}
+             2: "+ satisfied wait and fence", 3: "dQ loop: SS, TS, SS",
+             4: "3 accumulators, random operands", 7: "dQ loop, random operands",
+             2 | 8: "wait without fence", 2 | 16: "fence without wait",
+             2 | 24: "wait early, fence after chain", 3 | 24: "dQ loop, wait early",
+             2 | 32: "wait + fence, whole warp", 3 | 32: "dQ loop, whole warp",
+             2 | 64: "wait + fence, run-time offsets", 3 | 64: "dQ loop, run-time offsets",
+             2 | 96: "whole warp, run-time offsets", 3 | 96: "dQ loop, warp, run-time offsets",
+             3 | 120: "dQ loop, warp, rt off, early"}
     res = {}
     for ctas, n_iter in ((1, 32), (n_sm, 32), (n_sm, 2048)):
         for mode in names:
