@@ -50,9 +50,25 @@ static __device__ unsigned long long g_trace[kTraceSlots][kTraceLen];
     do {                                                                           \
         if (blockIdx.x == 0 && (idx) < kTraceLen) g_trace[slot][idx] = clock64(); \
     } while (0)
+// Per-CTA timeline: [kernel 0 = dK/dV, 1 = dQ][CTA][SM id, entry, end of MMA issue, exit], in
+// global-timer nanoseconds.
+__device__ __forceinline__ unsigned sm_id() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+constexpr int kCtaTraceMax = 8192;
+static __device__ unsigned long long g_cta_trace[2][kCtaTraceMax][4];
+#define FA_CTA_EVENT(kern, slot, value)                                               \
+    do {                                                                              \
+        if (blockIdx.x < kCtaTraceMax) g_cta_trace[kern][blockIdx.x][slot] = (value); \
+    } while (0)
 #else
 #define FA_TRACE_EVENT(slot, idx) \
     do {                          \
+    } while (0)
+#define FA_CTA_EVENT(kern, slot, value) \
+    do {                                \
     } while (0)
 #endif
 
@@ -95,8 +111,9 @@ struct DkvCfg {
     static constexpr int kQRingOff = 2 * kKVBytes;
     static constexpr int kDORingOff = kQRingOff + kQStages * kQStageBytes;
     static constexpr int kBarOff = kDORingOff + kDOStages * kQBytes;
-    // kv_full, q_full[], q_empty[], do_full[], do_empty[], s_full, dp_full, p_full, ds_full, dkv_full, mma_done
-    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 6;
+    // kv_full, q_full[], q_empty[], do_full[], do_empty[], s_full, dp_full, p_full, ds_full, dkv_full, mma_done,
+    // epi[2]
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 8;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kPayload = kMiscOff + 16;   // + TMEM address slot, abort flag
     static constexpr int kSlack = (kPayload + 1024 <= kSmemLimit) ? 1024 : 0;
@@ -261,12 +278,17 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                        BwdParams p) {
     using C = DkvCfg<D>;
     constexpr int BM = C::BM;
     constexpr int NQS = C::kQStages, NDS = C::kDOStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_window<C::kSlack>(smem_raw);
+    if (threadIdx.x == 0) {
+        FA_CTA_EVENT(0, 0, sm_id());
+        FA_CTA_EVENT(0, 1, globaltimer_ns());
+    }
     const uint32_t sbase = smem_u32(smem);
     if constexpr (C::kSlack == 0) {
         if (sbase & 1023u) {
@@ -292,6 +314,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t ds_full = b0 + 24;   // dS^T(i) written over dP^T(i)      (8 compute warps)
     const uint32_t dkv_full = b0 + 32;  // every dK / dV MMA done
     const uint32_t mma_done = b0 + 40;
+    auto epi_bar = [&](int hh) { return b0 + 48 + 8u * hh; };  // warpgroup hh staged its output (4 warps)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
     const Ctl ctl{abort_flag, p.timeout_ns};
@@ -330,6 +353,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(ds_full, 8);
         mbar_init(dkv_full, 1);
         mbar_init(mma_done, 1);
+        mbar_init(epi_bar(0), 4);
+        mbar_init(epi_bar(1), 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -467,6 +492,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             if (leader) mma_commit(dkv_full);
         mma_teardown:
+            FA_CTA_EVENT(0, 2, globaltimer_ns());
             if (leader) {
                 mma_commit(mma_done);
                 volatile int never = 0;
@@ -596,31 +622,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(ds_full);
             if (warp == 0 && lane == 0) FA_TRACE_EVENT(6, it);
         }
-        // epilogue: warpgroup 0 stores dK * scale, warpgroup 1 stores dV
+        // epilogue: warpgroup 0 stores dK * scale, warpgroup 1 stores dV.  Each
+        // stages its 128 x D bf16 tile in shared memory in the 128-byte swizzled
+        // layout of the tensor maps (dK in Q ring stage 0, dV in dO ring stage 0:
+        // every MMA has completed, so nothing reads them any more) and one
+        // thread writes it out with TMA stores, which clip rows past T.
         if (ok && warp_wait(dkv_full, 0, ctl)) {
             tc_fence_after();
-            const int key = kt * kBN + 32 * wq + lane;  // 32x32b shape: this thread's own lane
+            const uint32_t row = 32u * wq + lane;  // 32x32b shape: this thread's own lane (key row)
             const uint32_t col = h ? C::kDV : C::kDK;
             const float mul = h ? 1.f : p.scale;
-            __nv_bfloat16* out = h ? p.dv : p.dk;
+            const uint32_t stage = h ? sdO(0) : sQ(0);
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t v[32];
                 tmem_ld32(lane_base + col + 32 * ch, v);
                 tmem_ld_wait();
                 reg_fence32(v);
-                if (key < T) {
-                    uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * T + key) * D + 32 * ch);
+                const uint32_t atom = stage + (ch >> 1) * (BM * 128);
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]) * mul, __uint_as_float(v[8 * g + 1]) * mul);
-                        w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]) * mul, __uint_as_float(v[8 * g + 3]) * mul);
-                        w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]) * mul, __uint_as_float(v[8 * g + 5]) * mul);
-                        w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]) * mul, __uint_as_float(v[8 * g + 7]) * mul);
-                        dst[g] = w;
-                    }
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w4[e] = pack_bf16x2(__uint_as_float(v[8 * g + 2 * e]) * mul,
+                                            __uint_as_float(v[8 * g + 2 * e + 1]) * mul);
+                    st_shared_v4(atom + sw128_off(row, (ch & 1) * 4 + g), w4[0], w4[1], w4[2], w4[3]);
                 }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_bar(h));
+            if (wq == 0 && lane == 0 && wait_bar(epi_bar(h), 0, ctl)) {
+                for (int a = 0; a < C::kAtomsD; ++a)
+                    tma_store_3d(h ? &tm_dv : &tm_dk, stage + a * (BM * 128), 64 * a, kt * kBN, bh);
+                bulk_commit();
+                bulk_wait0();
             }
         }
     }
@@ -630,6 +667,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+        if (lane == 0) FA_CTA_EVENT(0, 3, globaltimer_ns());
     }
 }
 
@@ -655,6 +693,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr int NKS = C::kKStages, NVS = C::kVStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_window<C::kSlack>(smem_raw);
+    if (threadIdx.x == 0) {
+        FA_CTA_EVENT(1, 0, sm_id());
+        FA_CTA_EVENT(1, 1, globaltimer_ns());
+    }
     const uint32_t sbase = smem_u32(smem);
     if constexpr (C::kSlack == 0) {
         if (sbase & 1023u) {
@@ -864,6 +906,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ++item_no;
             }
         mma_teardown:
+            FA_CTA_EVENT(1, 2, globaltimer_ns());
             if (leader) {
                 mma_commit(mma_done);
                 volatile int never = 0;
@@ -988,6 +1031,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+        if (lane == 0) FA_CTA_EVENT(1, 3, globaltimer_ns());
     }
 }
 
@@ -1003,7 +1047,8 @@ bool set_smem_once(K kern, int bytes, bool& done) {
 
 template <int D, bool CAUSAL>
 int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                  BwdParams p, int BHq, int BHkv, cudaStream_t st, const DebugKnobs& dbg, int num_sms) {
+                  const CUtensorMap& tdk, const CUtensorMap& tdv, BwdParams p, int BHq, int BHkv, cudaStream_t st,
+                  const DebugKnobs& dbg, int num_sms) {
     static bool attr_a = false, attr_b = false;
     auto ka = fa_bwd_dkdv_kernel<D, CAUSAL>;
     auto kb = fa_bwd_dq_kernel<D, CAUSAL>;
@@ -1015,7 +1060,7 @@ int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     // 0.86 -> 0.71 ms, D = 64 T = 2048 0.129 -> 0.114 ms); head major above
     // (T = 8192, 32 heads: 0.771 vs 0.792 ms key-tile major)
     p.kt_major = (p.n_kt * BHkv < 8 * num_sms) ? 1 : 0;
-    ka<<<p.n_kt * BHkv, kBwdThreads, DkvCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, p);
+    ka<<<p.n_kt * BHkv, kBwdThreads, DkvCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, p);
     if (cudaGetLastError() != cudaSuccess) return -5;
     if (dbg.ev[3]) cudaEventRecord(dbg.ev[3], st);
     p.BH = BHq;
@@ -1037,9 +1082,10 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     const size_t bytes_vec = (static_cast<size_t>(BH) * T_pad * 4 + 255) / 256 * 256;
     float* dvec = static_cast<float*>(ws);
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_vec);
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
     if (!make_tmap_bhtd(&tq, q, BH, T, D, 128) || !make_tmap_bhtd(&tk, k, BHkv, T, D, 128) ||
-        !make_tmap_bhtd(&tv, v, BHkv, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, 128))
+        !make_tmap_bhtd(&tv, v, BHkv, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, 128) ||
+        !make_tmap_bhtd(&tdk, dk, BHkv, T, D, 128) || !make_tmap_bhtd(&tdv, dv, BHkv, T, D, 128))
         return -5;
     const long long rows = static_cast<long long>(BH) * T_pad;
     const long long blocks = (rows * (D / 8) + 255) / 256;
@@ -1074,10 +1120,10 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     p.sl2_eff = p.prescale ? 1.f : p.sl2;
     p.timeout_ns = dbg.timeout_ns;
     if (D == 64)
-        return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, p, BH, BHkv, stream, dbg, num_sms)
-                      : launch_main_t<64, false>(tq, tk, tv, tdo, p, BH, BHkv, stream, dbg, num_sms);
-    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, p, BH, BHkv, stream, dbg, num_sms)
-                  : launch_main_t<128, false>(tq, tk, tv, tdo, p, BH, BHkv, stream, dbg, num_sms);
+        return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms)
+                      : launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms);
+    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms)
+                  : launch_main_t<128, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms);
 }
 
 }  // namespace
@@ -1145,6 +1191,10 @@ int launch_bwd_noalloc(const void* q, const void* k, const void* v, const void* 
 // Copies the trace of the last traced launch (kTraceSlots x kTraceLen cycle stamps).
 extern "C" int fa_trace_read(unsigned long long* host) {
     return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -5;
+}
+// Copies the per-CTA timelines (2 x kCtaTraceMax x 4 values).
+extern "C" int fa_cta_trace_read(unsigned long long* host) {
+    return cudaMemcpyFromSymbol(host, g_cta_trace, sizeof(g_cta_trace)) == cudaSuccess ? 0 : -5;
 }
 #endif
 
