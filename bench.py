@@ -2,13 +2,15 @@
 """Throughput of the exact-attention hot path on GB300.
 
 One step = fa_fwd + fa_bwd (the whole path: forward with LSE, backward
-preprocess, fused key-outer backward, dQ conversion) over one batch of the
+preprocess, the dK/dV kernel with key tiles outer and the dQ kernel with
+query tiles outer) over one batch of the
 long-context causal workload B=2, H=16, T=8192, D=128 (bf16, seeded
 synthetic inputs resident in HBM).  FLOPs are counted as the pages count
 them: forward 4*B*H*T^2*D, halved under causal masking; backward 2.5x the
 forward.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+  python bench.py --configs | --sweep | --gqa | --varlen | --decode   (one line per case)
 
 N > 1 runs under torch.distributed.run: every rank processes its own
 independent batch (replicas, no collective on the data path); the barrier and
@@ -66,6 +68,9 @@ def parse_args():
     ap.add_argument("--varlen", action="store_true",
                     help="packed variable-length forward: 48 causal requests of 128..8192 tokens, H=16, D=128, "
                          "against the same batch padded to the longest request")
+    ap.add_argument("--configs", action="store_true",
+                    help="every specified workload (fwd, bwd; the small forward also with a cold L2): one JSON line per case")
+    ap.add_argument("--only", default=None, help="with --configs: run this workload only")
     ap.add_argument("--sweep", action="store_true",
                     help="T sweep (512..8192 at 16384 tokens x 16 heads): one JSON line per case, not the bench line")
     return ap.parse_args()
@@ -220,12 +225,70 @@ def run_reference(args, w, causal, rank, world):
 def algorithmic_bytes(B, H, T, D, bwd):
     """Bytes the pass must move at least: each tensor read or written once.
     Forward: read Q, K, V; write O (bf16) and LSE (fp32).  Backward: read Q,
-    K, V, O, dO, LSE; write dQ, dK, dV; plus the fp32 workspace (D and LSE2
-    written and read, dQ accumulator zeroed, reduced into and read)."""
+    K, V, O, dO, LSE; write dQ, dK, dV; plus the fp32 per-row workspace (D
+    and the log2-scaled LSE, each written once and read once)."""
     n = B * H * T * D
     if not bwd:
         return 2 * 4 * n + 4 * B * H * T
-    return 2 * 8 * n + 4 * B * H * T + 4 * 4 * B * H * T + 4 * 3 * n
+    return 2 * 8 * n + 4 * B * H * T + 4 * 4 * B * H * T
+
+
+def run_configs(args):
+    """Every specified workload, forward and (where specified) backward: median
+    over at least 20 launches after 5 warm-ups, each between its own pair of
+    events.  The small
+    non-causal forward (B=1 H=8 T=1024 D=64) is also timed with a 256 MB write
+    between launches, so it starts with a cold L2.  One JSON line per case."""
+    import torch
+    import online_softmax_05_gb300 as fa
+    from online_softmax_05_gb300.inputs import WORKLOADS, workload_inputs
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, src = load_peaks()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    n_iter = max(20, min(args.steps, 100))
+    for name, w in WORKLOADS.items():
+        if args.only and name != args.only:
+            continue
+        q, k, v, do = (t.to(dev) for t in workload_inputs(w))
+        B, H, T, D, sc = w.B, w.H, w.T, w.D, w.scale
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, T, device=dev)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        for causal in w.causal:
+            f = lambda: fa.fa_fwd(q, k, v, o, lse, B, H, T, D, sc, int(causal), stream)
+            b = lambda: fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, T, D, sc, int(causal), stream)
+            passes = [("fwd", f, False)] + ([("bwd", b, False)] if w.bwd else [])
+            if name == "fwd_b1h8t1024d64":
+                passes.append(("fwd", f, True))
+            fwd_fl = 4.0 * B * H * T * T * D / (2 if causal else 1)
+            for pname, fn, flush in passes:
+                for _ in range(max(5, args.warmup)):
+                    assert fn() == 0
+                torch.cuda.synchronize(dev)
+                # all launches enqueued back to back with an event pair around each,
+                # so host-side launch work is hidden and each pair times the GPU only
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(n_iter)]
+                for e0, e1 in evs:
+                    if flush:
+                        flush_buf.fill_(1)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                torch.cuda.synchronize(dev)
+                times = [e0.elapsed_time(e1) for e0, e1 in evs]
+                assert fa.fa_get_device_status(stream) == 0
+                ms = sorted(times)[len(times) // 2]
+                bwd = pname == "bwd"
+                fl = fwd_fl * (2.5 if bwd else 1.0)
+                nbytes = algorithmic_bytes(B, H, T, D, bwd)
+                print(json.dumps({"config": name, "pass": pname, "causal": bool(causal), "l2": "flushed" if flush else "warm",
+                                  "B": B, "H": H, "T": T, "D": D, "ms": ms, "tflops": fl / ms / 1e9,
+                                  "frac_of_burst": fl / ms / 1e9 / peaks["bf16_tflops"], "gbs": nbytes / ms / 1e6,
+                                  "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"], "iters": n_iter,
+                                  "peaks": src, "dtype": "bf16", "data": "synthetic"}), flush=True)
 
 
 def run_sweep(args):
@@ -413,6 +476,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.configs:
+        run_configs(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -174,6 +174,7 @@ struct BwdParams {
     __nv_bfloat16* dv;
     int T, T_pad, n_kt;   // n_kt = 128-row tiles (key tiles = query tiles)
     int kt_major;         // dK/dV kernel: CTA order key tile major (else head major)
+    int dq_pairs;         // dQ kernel: head-pair schedule (else heaviest first)
     int BH;               // rows of the grid: B*Hkv (dK/dV kernel) or B*Hq (dQ kernel)
     int Hq, Hkv, group;   // query heads, key/value heads, Hq / Hkv
     float scale;
@@ -672,16 +673,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ kernel
-// Work item w of a CTA (persistent grid, one CTA per SM): the items are
-// (query tile, query head), heaviest query tiles first across all heads (more
-// key tiles under causal masking); CTA b takes items b, 2G-1-b, 2G+b, ...
-// (snake order), which balances the heavy and light tiles.  Measured against
-// a head-major order and against groups of 4, 8 or 16 heads (better L2 reuse
-// of K and V), the balance wins.
-__device__ __forceinline__ int dq_item_of(int k, int n_items) {
-    const int G = gridDim.x;
-    const int w = k * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
-    return w < n_items ? w : -1;
+// The k-th (query tile, query head) item of this CTA (persistent grid, one CTA
+// per SM, G CTAs).  Returns 1 with (bh, qt), 0 for an empty slot (skip it), -1
+// when the CTA has no more work.  Two schedules:
+//   heaviest first  the items by query tile, heaviest first across all heads
+//                   (more key tiles under causal masking); CTA b takes items
+//                   b, 2G-1-b, 2G+b, ... (snake order), which balances heavy
+//                   and light tiles.  Every head's K and V are in flight at
+//                   once.  Measured against a head-major order and against
+//                   groups of 4, 8 or 16 heads under causal masking, the
+//                   balance wins.
+//   head pairs      units of two query tiles of one head, n_kt-1-r and r (equal
+//                   weight without masking, and under causal masking too: the
+//                   key-tile counts sum to n_kt + 1).  Units go head by head,
+//                   unit u to CTA u % G, so the units in flight cover about
+//                   G / (n_kt / 2) heads and their K and V stay in L2.
+// (Under causal masking only heaviest first is compiled.)
+template <bool CAUSAL>
+__device__ __forceinline__ int dq_item_of(int k, const BwdParams& p, int& bh, int& qt) {
+    const int G = gridDim.x, cta = static_cast<int>(blockIdx.x);
+    if (CAUSAL || !p.dq_pairs) {
+        const int w = k * G + ((k & 1) ? (G - 1 - cta) : cta);
+        if (w >= p.n_items) return -1;
+        bh = w % p.BH;
+        qt = p.n_kt - 1 - w / p.BH;
+        return 1;
+    }
+    const int U = (p.n_kt + 1) / 2;  // units per head
+    const int u = (k >> 1) * G + cta;
+    if (u >= p.BH * U) return -1;
+    bh = u / U;
+    const int r = u % U, heavy = p.n_kt - 1 - r;
+    if ((k & 1) == 0) {
+        qt = heavy;
+        return 1;
+    }
+    if (r == heavy) return 0;  // odd tile count: the middle tile has no partner
+    qt = r;
+    return 1;
 }
 
 template <int D, bool CAUSAL>
@@ -729,10 +758,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     struct Item {
         int bh, qt, bh_kv, n;
     };
-    auto item = [&](int w) {
+    auto item = [&](int bh, int qt) {
         Item it;
-        it.bh = w % p.BH;
-        it.qt = p.n_kt - 1 - w / p.BH;
+        it.bh = bh;
+        it.qt = qt;
         it.bh_kv = (it.bh / p.Hq) * p.Hkv + (it.bh % p.Hq) / p.group;
         it.n = fwd_num_kv_tiles(T, CAUSAL, it.qt);  // key tiles this query tile sees
         return it;
@@ -775,9 +804,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t pol_kv = l2_policy_evict_last();   // K, V of a head serve all its query tiles
             const uint64_t pol_q = l2_policy_evict_first();
             for (int k = 0;; ++k) {
-                const int w = dq_item_of(k, p.n_items);
-                if (w < 0) break;
-                const Item it = item(w);
+                int w_bh, w_qt;
+                const int got = dq_item_of<CAUSAL>(k, p, w_bh, w_qt);
+                if (got < 0) break;
+                if (got == 0) continue;
+                const Item it = item(w_bh, w_qt);
                 if (!wait_bar(qdo_empty, (qf & 1) ^ 1, ctl)) break;
                 mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
                 ++qf;
@@ -866,9 +897,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             //   S(j+2)                     into the buffer of S(j) (dQ(j) was its last reader)
             // The compute warps turn S(j+1) and dP(j+1) into dS(j+1) while these run.
             for (int k = 0;; ++k) {
-                const int w = dq_item_of(k, p.n_items);
-                if (w < 0) break;
-                const Item it = item(w);
+                int w_bh, w_qt;
+                const int got = dq_item_of<CAUSAL>(k, p, w_bh, w_qt);
+                if (got < 0) break;
+                if (got == 0) continue;
+                const Item it = item(w_bh, w_qt);
                 if (!wait_all(qdo_full, qc & 1, ctl)) goto mma_teardown;
                 ++qc;
                 tc_fence_after();
@@ -926,9 +959,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t eff2 = f2(eff, eff);
         uint32_t sc = 0, vc = 0, item_no = 0;  // S and dP numbers, items done: as in the MMA warp
         for (int k = 0;; ++k) {
-            const int w = dq_item_of(k, p.n_items);
-            if (w < 0) break;
-            const Item it = item(w);
+            int w_bh, w_qt;
+            const int got = dq_item_of<CAUSAL>(k, p, w_bh, w_qt);
+            if (got < 0) break;
+            if (got == 0) continue;
+            const Item it = item(w_bh, w_qt);
             const int q = it.qt * 128 + r;
             // -LSE2 and -D of this row (0 on padded rows q >= T, which the mask zeroes anyway)
             const float nlse = p.lse2[static_cast<size_t>(it.bh) * p.T_pad + q];
@@ -1065,6 +1100,16 @@ int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     if (dbg.ev[3]) cudaEventRecord(dbg.ev[3], st);
     p.BH = BHq;
     p.n_items = p.n_kt * BHq;
+    {
+        // Head pairs without causal masking, when every head's K and V exceed
+        // half of L2 (~64 MB) and each CTA gets at least 4 units; heaviest
+        // first otherwise.  Measured: B=8 H=32 T=3000 D=128 non-causal backward
+        // 3.26 -> 3.01 ms; with causal masking (B=2 H=16 T=8192 D=128) the
+        // pairs made the dQ kernel slower (0.513 -> 0.557 ms).
+        const long long units = static_cast<long long>(BHq) * ((p.n_kt + 1) / 2);
+        const double kv_bytes = 2.0 * BHkv * static_cast<double>(p.T) * D * 2.0;
+        p.dq_pairs = (!CAUSAL && kv_bytes > 64e6 && units >= 4LL * num_sms) ? 1 : 0;
+    }
     const int grid_b = p.n_items < num_sms ? p.n_items : num_sms;  // persistent: one CTA per SM
     kb<<<grid_b, kBwdThreads, DqCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, p);
     if (cudaGetLastError() != cudaSuccess) return -5;
@@ -1110,6 +1155,7 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     p.T_pad = T_pad;
     p.n_kt = cdiv(T, kBN);
     p.kt_major = 0;
+    p.dq_pairs = 0;
     p.BH = BHkv;
     p.Hq = Hq;
     p.Hkv = Hkv;

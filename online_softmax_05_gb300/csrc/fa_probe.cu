@@ -272,7 +272,9 @@ __global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_i
     const uint32_t tslot = bar + 24;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool noisy = (mode & 4) != 0;
+    const int bg = (mode >> 3) & 3;  // 1: warps 1-3 stream TMEM loads; 2: shared-memory loads
     mode &= 3;
+    volatile int* done = reinterpret_cast<volatile int*>(smem + (tslot - sA) + 8);
     for (int i = tid; i < (2 * 128 * 128 * 2) / 4; i += 128) {
         uint32_t w = 0x3f803f80u;  // 1.0 in both halves
         if (noisy) {
@@ -294,6 +296,7 @@ __global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_i
         mbar_init(bar, 1);
         mbar_init(bar2, 1);
         mbar_init(bar3, 1);
+        *done = 0;
         fence_mbar_init();
     }
     fence_proxy_async_smem();
@@ -303,6 +306,30 @@ __global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_i
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tslot - sA));
     if (tid == 0) mbar_arrive(bar3);  // a phase that has completed: waits on it return at once
     __syncwarp();
+    if (warp != 0 && bg != 0) {
+        // background traffic until warp 0 is done (at most 2^20 rounds)
+        uint32_t acc = 0;
+        for (int it = 0; it < (1 << 20) && !*done; ++it) {
+            if (bg == 1) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((32u * warp) << 16) + 256u, r);
+                tmem_ld_wait();
+                reg_fence32(r);
+                acc ^= r[it & 31];
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t off = ((static_cast<uint32_t>(it) * 8u + u) * 512u + lane * 16u) & (65536u - 1u);
+                    uint32_t a, b, c, d;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                                 : "r"(sA + off));
+                    acc ^= a ^ b ^ c ^ d;
+                }
+            }
+        }
+        if (acc == 0x12345678u) *done = 2;  // keeps the loads
+    }
     if (warp == 0 && (WIDE || lane == 0)) {
         const bool leader = WIDE ? elect_one_sync() : true;
         const uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
@@ -359,6 +386,7 @@ __global__ void __launch_bounds__(128, 1) probe_mma_seq_kernel(int mode, int n_i
         if (leader) mma_commit(bar);
         probe_wait(bar, 0, err);
         if (lane == 0) out[0] = clock64() - t0;
+        *done = 1;
     }
     __syncwarp();
     tc_fence_before();
@@ -503,9 +531,10 @@ int probe_mma_chain(int N, int n, int chain, int kind, long long* out_host) {
 
 // ctas: number of CTAs (one per SM at this shared-memory size) running the
 // same sequence at once; out_host receives one count per CTA.
-// mode bits: 0-1 loop, 2 random operands, 3-4 SYNC, 5 WIDE, 6 RTOFF (see probe_mma_seq_kernel)
+// mode bits: 0-1 loop, 2 random operands, 3-4 SYNC, 5 WIDE, 6 RTOFF, 7-8 background traffic
+// (1 TMEM loads, 2 shared-memory loads by warps 1-3; see probe_mma_seq_kernel)
 int probe_mma_seq(int mode, int n_iter, int ctas, long long* out_host) {
-    if (mode < 0 || mode > 127 || n_iter < 1 || n_iter > 4096 || ctas < 1 || ctas > 1024) return -1;
+    if (mode < 0 || mode > 511 || ((mode >> 7) & 3) == 3 || n_iter < 1 || n_iter > 4096 || ctas < 1 || ctas > 1024) return -1;
     int* err = nullptr;
     long long* out = nullptr;
     if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) return -5;
@@ -521,7 +550,7 @@ int probe_mma_seq(int mode, int n_iter, int ctas, long long* out_host) {
         fa::launch_seq<2, false, true>,  fa::launch_seq<2, true, false>,  fa::launch_seq<2, true, true>,
         fa::launch_seq<3, false, false>, fa::launch_seq<3, false, true>,  fa::launch_seq<3, true, false>,
         fa::launch_seq<3, true, true>};
-    kSeq[((mode >> 3) & 3) * 4 + ((mode >> 5) & 1) * 2 + ((mode >> 6) & 1)](mode & 7, n_iter, out, err, ctas, smem);
+    kSeq[((mode >> 3) & 3) * 4 + ((mode >> 5) & 1) * 2 + ((mode >> 6) & 1)]((mode & 7) | (((mode >> 7) & 3) << 3), n_iter, out, err, ctas, smem);
     cudaError_t e = cudaDeviceSynchronize();
     int h = 0;
     cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost);

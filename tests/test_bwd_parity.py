@@ -104,3 +104,25 @@ def test_backward_workload_sampled_rows(name):
         check(f"dq[{bh}]", dq[b, h, rows], rq)
         check(f"dk[{bh}]", dk[b, h, rows], rk)
         check(f"dv[{bh}]", dv[b, h, rows], rv)
+
+
+@pytest.mark.gpu
+def test_backward_head_pair_schedule_odd_tile_count():
+    # Non-causal, K and V of all heads well above half of L2: the dQ kernel
+    # walks (tile n-1-r, tile r) pairs head by head.  T = 2900 gives 23 query
+    # tiles, so tile 11 has no partner; rows of every tile boundary and of the
+    # unpaired tile are compared, on the first, a middle and the last head.
+    B, H, T, D = 8, 32, 2900, 128
+    q, k, v, do = make_inputs(B, H, T, D, seed=29)
+    scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = run_fwd_bwd(q, k, v, do, False, scale)
+    rng = np.random.default_rng(11)
+    middle = 11 * 128
+    for bh in (0, B * H // 2 + 3, B * H - 1):
+        b, h = divmod(bh, H)
+        rows = sorted({0, 127, 128, middle, middle + 77, middle + 127, T - 1} | set(rng.integers(0, T, 12).tolist()))
+        rq, rk, rv, _, _ = oracle.attn_bwd_rows(to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h]),
+                                                to_f64(do[b, h]), scale, False, rows, rows)
+        check(f"dq[{bh}]", dq[b, h, rows], rq)
+        check(f"dk[{bh}]", dk[b, h, rows], rk)
+        check(f"dv[{bh}]", dv[b, h, rows], rv)

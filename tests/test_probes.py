@@ -109,7 +109,8 @@ def test_mma_sequence_report(plib, capsys):
     fence alone, and the wait issued before the last two MMAs of the
     previous chain; then the loop run by the whole warp with elect.sync
     choosing the issuing lane, and descriptor offsets known only at run
-    time (as the kernels' ring stages are)."""
+    time (as the kernels' ring stages are); and the warp-wide dQ loop while
+    the other three warps stream TMEM loads or shared-memory loads."""
     import torch
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     plib.probe_mma_seq.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong)]
@@ -121,7 +122,8 @@ def test_mma_sequence_report(plib, capsys):
              2 | 32: "wait + fence, whole warp", 3 | 32: "dQ loop, whole warp",
              2 | 64: "wait + fence, run-time offsets", 3 | 64: "dQ loop, run-time offsets",
              2 | 96: "whole warp, run-time offsets", 3 | 96: "dQ loop, warp, run-time offsets",
-             3 | 120: "dQ loop, warp, rt off, early"}
+             3 | 120: "dQ loop, warp, rt off, early",
+             3 | 96 | 128: "dQ loop (warp) + TMEM loads", 3 | 96 | 256: "dQ loop (warp) + smem loads"}
     res = {}
     for ctas, n_iter in ((1, 32), (n_sm, 32), (n_sm, 2048)):
         for mode in names:
