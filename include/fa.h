@@ -27,7 +27,8 @@
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream).  Calls are asynchronous: they enqueue kernels on `stream` and
  * return without synchronising.  fa_bwd takes its workspace (two vectors of
- * B*H*T_pad floats, T_pad = T rounded up to 128: D and log2-scaled LSE)
+ * B*H*T_pad floats, T_pad = T rounded up to 128: D and log2-scaled LSE, plus
+ * 256 bytes for a work counter)
  * stream-ordered with cudaMallocAsync on `stream` and releases it with
  * cudaFreeAsync on the same stream before returning.
  *
@@ -100,9 +101,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  *
  * Same arguments, layout, results and asynchrony as fa_bwd.  The caller
  * still owns every input and output.
- * Limit: 8 * B*H*T_pad bytes must not exceed the scratch size, where T_pad
- *   is T rounded up to a multiple of 128 (B*H*T_pad <= 8 M rows); larger
- *   problems return FA_ERR_SCRATCH and nothing is enqueued.
+ * Limit: 8 * B*H*T_pad + 256 bytes (each of the two vectors rounded up to
+ *   256 bytes) must not exceed the scratch size, where T_pad is T rounded up
+ *   to a multiple of 128 (B*H*T_pad just under 8 M rows); larger problems
+ *   return FA_ERR_SCRATCH and nothing is enqueued.
  * Set-up: the first call on each device looks up the buffer's device
  *   address (cudaGetSymbolAddress); make that first call before any stream
  *   capture.

@@ -147,10 +147,10 @@ struct DqCfg {
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
     // qdo_full, qdo_empty, k_full[], k_empty[], v_full[], v_empty[], s_full[2], dp_full, ds_full, dq_full,
-    // dq_empty, mma_done
-    static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 5;
+    // dq_empty, mma_done, item_full[4], item_empty[4]
+    static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 5 + 8;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kPayload = kMiscOff + 16;
+    static constexpr int kPayload = kMiscOff + 32;   // + TMEM address slot, abort flag, item ring (4 ints)
     static constexpr int kSlack = (kPayload + 1024 <= kSmemLimit) ? 1024 : 0;
     static constexpr int kSmemBytes = kPayload + kSlack;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
@@ -174,7 +174,7 @@ struct BwdParams {
     __nv_bfloat16* dv;
     int T, T_pad, n_kt;   // n_kt = 128-row tiles (key tiles = query tiles)
     int kt_major;         // dK/dV kernel: CTA order key tile major (else head major)
-    int dq_pairs;         // dQ kernel: head-pair schedule (else heaviest first)
+    int* dq_next;         // dQ kernel: next item to hand out (zeroed by the preprocess kernel)
     int BH;               // rows of the grid: B*Hkv (dK/dV kernel) or B*Hq (dQ kernel)
     int Hq, Hkv, group;   // query heads, key/value heads, Hq / Hkv
     float scale;
@@ -238,8 +238,10 @@ template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          const float* __restrict__ lse, float* __restrict__ dvec,
-                                                         float* __restrict__ lse2, int BH, int T, int T_pad) {
+                                                         float* __restrict__ lse2, int BH, int T, int T_pad,
+                                                         int* __restrict__ dq_next) {
     constexpr int TPR = D / 8;            // threads per row
+    if (blockIdx.x == 0 && threadIdx.x == 0) *dq_next = 0;  // the dQ kernel's item counter
     constexpr int RPW = 32 / TPR;         // rows per warp
     const long long total = static_cast<long long>(BH) * T_pad;
     const int lane = threadIdx.x & 31, sub = lane % TPR;
@@ -322,6 +324,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.T;
+    // The dQ grid needs nothing from this one: it may launch as soon as every
+    // CTA of this grid has started (its CTAs then fill SMs freed in the tail).
+    griddep_launch_dependents();
     // CTA order.  Head major: the key tiles of one head run together (their Q
     // and dO stay in L2), heavy key tiles first within a head.  Key tile
     // major: every head's heavy key tiles first, which shortens the causal
@@ -673,45 +678,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ kernel
-// The k-th (query tile, query head) item of this CTA (persistent grid, one CTA
-// per SM, G CTAs).  Returns 1 with (bh, qt), 0 for an empty slot (skip it), -1
-// when the CTA has no more work.  Two schedules:
-//   heaviest first  the items by query tile, heaviest first across all heads
-//                   (more key tiles under causal masking); CTA b takes items
-//                   b, 2G-1-b, 2G+b, ... (snake order), which balances heavy
-//                   and light tiles.  Every head's K and V are in flight at
-//                   once.  Measured against a head-major order and against
-//                   groups of 4, 8 or 16 heads under causal masking, the
-//                   balance wins.
-//   head pairs      units of two query tiles of one head, n_kt-1-r and r (equal
-//                   weight without masking, and under causal masking too: the
-//                   key-tile counts sum to n_kt + 1).  Units go head by head,
-//                   unit u to CTA u % G, so the units in flight cover about
-//                   G / (n_kt / 2) heads and their K and V stay in L2.
-// (Under causal masking only heaviest first is compiled.)
+// Work items are (query tile, query head) pairs, handed out one at a time from
+// a counter in global memory: a persistent CTA (one per SM) takes the next
+// item whenever it is ready for one, so the CTAs that start early (the grid
+// may launch during the dK/dV grid's tail) or draw light items do more of
+// them.  Item w in order:
+//   causal masking  heaviest query tiles first across all heads (a tile sees
+//                   more key tiles the later it is), which keeps the end of
+//                   the grid balanced;
+//   no masking      head by head (every item weighs the same), so the items in
+//                   flight cover a few heads and their K and V stay in L2.
 template <bool CAUSAL>
-__device__ __forceinline__ int dq_item_of(int k, const BwdParams& p, int& bh, int& qt) {
-    const int G = gridDim.x, cta = static_cast<int>(blockIdx.x);
-    if (CAUSAL || !p.dq_pairs) {
-        const int w = k * G + ((k & 1) ? (G - 1 - cta) : cta);
-        if (w >= p.n_items) return -1;
+__device__ __forceinline__ void dq_item_at(int w, const BwdParams& p, int& bh, int& qt) {
+    if constexpr (CAUSAL) {
         bh = w % p.BH;
         qt = p.n_kt - 1 - w / p.BH;
-        return 1;
+    } else {
+        bh = w / p.n_kt;
+        qt = w % p.n_kt;
     }
-    const int U = (p.n_kt + 1) / 2;  // units per head
-    const int u = (k >> 1) * G + cta;
-    if (u >= p.BH * U) return -1;
-    bh = u / U;
-    const int r = u % U, heavy = p.n_kt - 1 - r;
-    if ((k & 1) == 0) {
-        qt = heavy;
-        return 1;
-    }
-    if (r == heavy) return 0;  // odd tile count: the middle tile has no partner
-    qt = r;
-    return 1;
 }
+constexpr int kDqItemRing = 4;  // item numbers passed from the producer to the other roles
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -749,8 +736,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t dq_full = b0 + 32;                   // every dQ MMA of the item done
     const uint32_t dq_empty = b0 + 40;                  // dQ read out of TMEM (8 warps)
     const uint32_t mma_done = b0 + 48;
+    // item ring: the producer writes item numbers, the MMA warp and the 8 compute warps read them
+    auto item_full = [&](int i) { return b0 + 56 + 8u * i; };
+    auto item_empty = [&](int i) { return b0 + 56 + 8u * (kDqItemRing + i); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+    volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 16);
     const Ctl ctl{abort_flag, p.timeout_ns};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -785,6 +776,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, 8);
         mbar_init(mma_done, 1);
+        for (int i = 0; i < kDqItemRing; ++i) {
+            mbar_init(item_full(i), 1);
+            mbar_init(item_empty(i), 9);  // the MMA warp and the 8 compute warps
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -804,10 +799,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t pol_kv = l2_policy_evict_last();   // K, V of a head serve all its query tiles
             const uint64_t pol_q = l2_policy_evict_first();
             for (int k = 0;; ++k) {
+                // take the next item and pass its number on (a number past the
+                // last item tells the other roles to stop)
+                const int slot = k % kDqItemRing;
+                if (!wait_bar(item_empty(slot), ((k / kDqItemRing) & 1) ^ 1, ctl)) break;
+                const int w = atomicAdd(p.dq_next, 1);
+                item_ring[slot] = w;
+                mbar_arrive(item_full(slot));
+                if (w >= p.n_items) break;
                 int w_bh, w_qt;
-                const int got = dq_item_of<CAUSAL>(k, p, w_bh, w_qt);
-                if (got < 0) break;
-                if (got == 0) continue;
+                dq_item_at<CAUSAL>(w, p, w_bh, w_qt);
                 const Item it = item(w_bh, w_qt);
                 if (!wait_bar(qdo_empty, (qf & 1) ^ 1, ctl)) break;
                 mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
@@ -897,10 +898,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             //   S(j+2)                     into the buffer of S(j) (dQ(j) was its last reader)
             // The compute warps turn S(j+1) and dP(j+1) into dS(j+1) while these run.
             for (int k = 0;; ++k) {
+                const int slot = k % kDqItemRing;
+                if (!wait_all(item_full(slot), (k / kDqItemRing) & 1, ctl)) goto mma_teardown;
+                const int w = item_ring[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(item_empty(slot));
+                if (w >= p.n_items) break;
                 int w_bh, w_qt;
-                const int got = dq_item_of<CAUSAL>(k, p, w_bh, w_qt);
-                if (got < 0) break;
-                if (got == 0) continue;
+                dq_item_at<CAUSAL>(w, p, w_bh, w_qt);
                 const Item it = item(w_bh, w_qt);
                 if (!wait_all(qdo_full, qc & 1, ctl)) goto mma_teardown;
                 ++qc;
@@ -959,10 +964,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t eff2 = f2(eff, eff);
         uint32_t sc = 0, vc = 0, item_no = 0;  // S and dP numbers, items done: as in the MMA warp
         for (int k = 0;; ++k) {
+            const int slot = k % kDqItemRing;
+            if (!wait_all(item_full(slot), (k / kDqItemRing) & 1, ctl)) goto compute_done;
+            const int w = item_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(item_empty(slot));
+            if (w >= p.n_items) break;
             int w_bh, w_qt;
-            const int got = dq_item_of<CAUSAL>(k, p, w_bh, w_qt);
-            if (got < 0) break;
-            if (got == 0) continue;
+            dq_item_at<CAUSAL>(w, p, w_bh, w_qt);
             const Item it = item(w_bh, w_qt);
             const int q = it.qt * 128 + r;
             // -LSE2 and -D of this row (0 on padded rows q >= T, which the mask zeroes anyway)
@@ -1068,6 +1077,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_dealloc(tmem, 512);
         if (lane == 0) FA_CTA_EVENT(1, 3, globaltimer_ns());
     }
+    // This grid may have started while the dK/dV grid was still running (the
+    // two read the same inputs and write disjoint outputs).  It ends only after
+    // that grid has, so work after this launch sees dK and dV complete.
+    griddep_wait();
 }
 
 template <typename K>
@@ -1100,25 +1113,30 @@ int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     if (dbg.ev[3]) cudaEventRecord(dbg.ev[3], st);
     p.BH = BHq;
     p.n_items = p.n_kt * BHq;
-    {
-        // Head pairs without causal masking, when every head's K and V exceed
-        // half of L2 (~64 MB) and each CTA gets at least 4 units; heaviest
-        // first otherwise.  Measured: B=8 H=32 T=3000 D=128 non-causal backward
-        // 3.26 -> 3.01 ms; with causal masking (B=2 H=16 T=8192 D=128) the
-        // pairs made the dQ kernel slower (0.513 -> 0.557 ms).
-        const long long units = static_cast<long long>(BHq) * ((p.n_kt + 1) / 2);
-        const double kv_bytes = 2.0 * BHkv * static_cast<double>(p.T) * D * 2.0;
-        p.dq_pairs = (!CAUSAL && kv_bytes > 64e6 && units >= 4LL * num_sms) ? 1 : 0;
-    }
     const int grid_b = p.n_items < num_sms ? p.n_items : num_sms;  // persistent: one CTA per SM
-    kb<<<grid_b, kBwdThreads, DqCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, p);
+    {
+        // programmatic dependent launch: the dQ grid may start during the dK/dV
+        // grid's tail (it waits for that grid only before it exits)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid_b);
+        cfg.blockDim = dim3(kBwdThreads);
+        cfg.dynamicSmemBytes = DqCfg<D>::kSmemBytes;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kb, tq, tk, tv, tdo, p) != cudaSuccess) return -5;
+    }
     if (cudaGetLastError() != cudaSuccess) return -5;
     if (dbg.ev[4]) cudaEventRecord(dbg.ev[4], st);
     return 0;
 }
 
 // Preprocess + both main kernels, with the workspace (two vectors of
-// B*Hq*T_pad floats at ws, the second 256-byte aligned) already in place.
+// B*Hq*T_pad floats at ws, each 256-byte aligned, then the dQ kernel's item
+// counter) already in place.
 int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
             void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, bool causal, void* ws,
             cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
@@ -1127,6 +1145,7 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     const size_t bytes_vec = (static_cast<size_t>(BH) * T_pad * 4 + 255) / 256 * 256;
     float* dvec = static_cast<float*>(ws);
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_vec);
+    int* dq_next = reinterpret_cast<int*>(static_cast<char*>(ws) + 2 * bytes_vec);
     CUtensorMap tq, tk, tv, tdo, tdk, tdv;
     if (!make_tmap_bhtd(&tq, q, BH, T, D, 128) || !make_tmap_bhtd(&tk, k, BHkv, T, D, 128) ||
         !make_tmap_bhtd(&tv, v, BHkv, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, 128) ||
@@ -1138,15 +1157,16 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     if (D == 64)
         fa_bwd_pre_kernel<64><<<pre_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                             static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2,
-                                                            BH, T, T_pad);
+                                                            BH, T, T_pad, dq_next);
     else
         fa_bwd_pre_kernel<128><<<pre_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                              static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2,
-                                                             BH, T, T_pad);
+                                                             BH, T, T_pad, dq_next);
     if (cudaGetLastError() != cudaSuccess) return -5;
     BwdParams p;
     p.lse2 = lse2;
     p.dvec = dvec;
+    p.dq_next = dq_next;
     p.dq = static_cast<__nv_bfloat16*>(dq);
     p.n_items = 0;
     p.dk = static_cast<__nv_bfloat16*>(dk);
@@ -1155,7 +1175,6 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     p.T_pad = T_pad;
     p.n_kt = cdiv(T, kBN);
     p.kt_major = 0;
-    p.dq_pairs = 0;
     p.BH = BHkv;
     p.Hq = Hq;
     p.Hkv = Hkv;
@@ -1179,7 +1198,7 @@ size_t bwd_scratch_bytes(int B, int H, int T, int D) {
     const size_t BH = static_cast<size_t>(B) * H;
     const size_t T_pad = static_cast<size_t>(cdiv(T, 128)) * 128;
     const size_t bytes_vec = (BH * T_pad * 4 + 255) / 256 * 256;
-    return 2 * bytes_vec;
+    return 2 * bytes_vec + 256;  // + the dQ kernel's item counter
 }
 
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,

@@ -262,6 +262,14 @@ __device__ __forceinline__ SDesc sdesc_make(uint32_t saddr, uint32_t lbo_bytes, 
     const uint64_t d = sdesc_sw128(saddr, lbo_bytes, sbo_bytes);
     return SDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
 }
+// Programmatic dependent launch: let the next grid in the stream start once
+// every CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on have completed and their memory
+// operations are visible (returns at once for a normally launched grid).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // One lane of the converged warp (the lowest active one) gets true.
 __device__ __forceinline__ bool elect_one_sync() {
     uint32_t ok;
