@@ -76,6 +76,29 @@ def parse_args():
     return ap.parse_args()
 
 
+def rank_seed(w, rank):
+    """Each rank draws its own batch (replicas: no collective on the data path);
+    rank 0's batch is the single-GPU one."""
+    return w.seed + rank
+
+
+def reduce_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum over ranks (the slowest rank sets every time), or
+    the values unchanged without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(world, step_flops, ms):
+    """Whole-job throughput: every rank processes one step's worth of units in
+    ms milliseconds (the maximum over ranks)."""
+    return world * step_flops / (ms * 1e-3) / 1e12
+
+
 def workload_flops(w, causal):
     fwd = 4.0 * w.B * w.H * w.T * w.T * w.D / (2.0 if causal else 1.0)
     return fwd, 2.5 * fwd
@@ -506,7 +529,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     # seeded inputs, one independent batch per rank, resident in HBM
-    q, k, v, do = (t.to(dev) for t in make_inputs(w.B, w.H, w.T, w.D, seed=w.seed + rank, qk_std=w.qk_std,
+    q, k, v, do = (t.to(dev) for t in make_inputs(w.B, w.H, w.T, w.D, seed=rank_seed(w, rank), qk_std=w.qk_std,
                                                    big_row_frac=w.big_row_frac, big_row_mult=w.big_row_mult))
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.T, device=dev, dtype=torch.float32)
@@ -572,15 +595,12 @@ def main():
     fwd_ms = statistics.mean(evs[s][0].elapsed_time(evs[s][1]) for s in range(KS))
     dkdv_ms = statistics.mean(evs[s][2].elapsed_time(evs[s][3]) for s in range(KS))
     dq_ms = statistics.mean(evs[s][3].elapsed_time(evs[s][4]) for s in range(KS))
-    if dist is not None:
-        tt = torch.tensor([ms, fwd_ms, dkdv_ms, dq_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, fwd_ms, dkdv_ms, dq_ms = tt.tolist()
+    ms, fwd_ms, dkdv_ms, dq_ms = reduce_over_ranks([ms, fwd_ms, dkdv_ms, dq_ms], dist, dev)
     bwd_ms = dkdv_ms + dq_ms
 
     fwd_fl, bwd_fl = workload_flops(w, causal)
     step_fl = fwd_fl + bwd_fl
-    value = world * step_fl / (ms * 1e-3) / 1e12
+    value = job_tflops(world, step_fl, ms)
     fwd_tflops_kernel = fwd_fl / (fwd_ms * 1e-3) / 1e12
     bwd_tflops_kernels = bwd_fl / (bwd_ms * 1e-3) / 1e12
     # Algorithmic FLOPs per backward kernel: of the backward's five products
@@ -663,14 +683,10 @@ def main():
         e2e_run(n_e2e)
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = a.elapsed_time(b) / n_e2e
-        if dist is not None:
-            tt = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = tt.item()
+        e_ms = reduce_over_ranks([a.elapsed_time(b) / n_e2e], dist, dev)[0]
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
         d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
-        e2e = {"value": world * step_fl / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+        e2e = {"value": job_tflops(world, step_fl, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
                "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "copies": "upload and download streams, two device buffer sets, overlapped with the kernels"}
 
