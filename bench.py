@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "attention TFLOP/s fwd & fwd+bwd (bf16, 1×GB300) and % of dense BF16 peak"
 DEFAULT_WORKLOAD = "causal_b2h16t8192d128"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+DATASHEET_BF16_TFLOPS = 2250.0  # vendor dense bf16 figure per GPU, reported beside the measured peaks only
 CLOCK_FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -716,7 +717,10 @@ def main():
                         "starts in the dK/dV grid's tail)",
         "pct_of_peak": {"fwd_bwd_of_burst": 100 * value / world / peak_burst,
                         "fwd_bwd_of_sustained": 100 * value / world / peak_sus,
-                        "fwd_of_burst": 100 * fwd_tflops_kernel / peak_burst, "peaks": peak_src},
+                        "fwd_of_burst": 100 * fwd_tflops_kernel / peak_burst, "peaks": peak_src,
+                        "fwd_bwd_of_datasheet": 100 * value / world / DATASHEET_BF16_TFLOPS,
+                        "datasheet": f"{DATASHEET_BF16_TFLOPS:.0f} TFLOP/s dense bf16 per GB300 (vendor figure, "
+                                     "not measured here)"},
         "roofline": rls[0][1],
         "roofline_other": [r for _, r in rls[1:]],
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * K,
