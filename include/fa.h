@@ -160,6 +160,28 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                   float scale, int causal, void* stream);
 
 /*
+ * Backward of fa_fwd_varlen over the same packed batch ("Triton
+ * FlashAttention-2 forward", "Exercises": the cu_seqlens packing; the
+ * gradients as in fa_bwd, "Lab 06 - Attention kernels", section 4).  Each
+ * sequence's gradients involve only its own rows.
+ *   q, k, v, o, dO in : (total, H, D) bf16, packed; o and lse from fa_fwd_varlen
+ *   lse            in : (H, total) float32
+ *   dq, dk, dv     out: (total, H, D) bf16
+ *   cu_seqlens, n_seq, max_seqlen, total: as in fa_fwd_varlen
+ * Workspace: like fa_bwd's, stream-ordered with cudaMallocAsync on `stream`:
+ * two vectors of H * n_seq * T_pad floats (T_pad = max_seqlen rounded up to
+ * 128) plus 256 bytes, released before returning.
+ * A length above max_seqlen (or negative) is reported as FA_ERR_SEQLEN by
+ * fa_get_device_status; that sequence's gradients are left unwritten.
+ * FA_ERR_ARG if an output overlaps an input or another output; other
+ * arguments and errors as in fa_fwd_varlen and fa_bwd.
+ */
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                  const float* lse, void* dq, void* dk, void* dv, const int* cu_seqlens,
+                  int n_seq, int max_seqlen, int total, int H, int D, float scale, int causal,
+                  void* stream);
+
+/*
  * Decoding forward, split over the keys ("Lab 06 - Attention kernels",
  * "Check yourself" item 2 and "Stretch": a few new query rows against a long
  * key/value cache).  Each of the Tq query rows of a head attends to ALL Tk

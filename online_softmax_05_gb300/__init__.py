@@ -12,7 +12,7 @@ import math
 import os
 import threading
 
-__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen", "attention_forward_varlen", "fa_decode", "attention_decode", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
+__all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen", "attention_forward_varlen", "fa_bwd_varlen", "attention_backward_varlen", "fa_decode", "attention_decode", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
            "attention_forward", "attention_backward", "FAError", "library_path", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -57,6 +57,8 @@ def load_library():
         lib.fa_bwd_gqa.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_varlen.restype = i
+        lib.fa_bwd_varlen.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, vp]
+        lib.fa_bwd_varlen.restype = i
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.fa_decode.restype = i
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -155,6 +157,37 @@ def attention_forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool 
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_varlen")
     return out, lse
+
+
+def fa_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, n_seq: int, max_seqlen: int, total: int, H: int,
+                  D: int, scale: float, causal: int, stream=None) -> int:
+    """C-ABI ``fa_bwd_varlen``: gradients of the packed-sequence forward."""
+    return load_library().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                                        _ptr(dv), _ptr(cu_seqlens), n_seq, max_seqlen, total, H, D, float(scale),
+                                        int(causal), _stream(stream))
+
+
+def attention_backward_varlen(q, k, v, o, lse, dO, cu_seqlens, max_seqlen: int, causal: bool = False,
+                              scale: float | None = None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV (total, H, D) for packed sequences (o, lse from attention_forward_varlen)."""
+    import torch
+    total, H, D = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 3):
+            raise ValueError(f"{n} must be a contiguous (total, H, D) bf16 CUDA tensor")
+    if not (cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous()):
+        raise ValueError("cu_seqlens must be a contiguous int32 CUDA tensor")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, cu_seqlens.numel() - 1, max_seqlen, total, H, D,
+                       scale, int(causal), stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd_varlen")
+    return dq, dk, dv
 
 
 def fa_decode(q, k, v, o, lse, B: int, H: int, Tq: int, Tk: int, D: int, scale: float, stream=None) -> int:

@@ -198,6 +198,38 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                                  static_cast<cudaStream_t>(stream), knobs(), sms);
 }
 
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens, int n_seq, int max_seqlen, int total, int H,
+                  int D, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !cu_seqlens) return FA_ERR_NULL;
+    if (n_seq < 1 || max_seqlen < 1 || total < 1 || H < 1) return FA_ERR_SHAPE;
+    if (static_cast<long long>(total) * H > INT_MAX || static_cast<long long>(n_seq) * H > (1 << 30) ||
+        static_cast<long long>(n_seq) * H * ((max_seqlen + 127) / 128) > INT_MAX)
+        return FA_ERR_SHAPE;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (causal != 0 && causal != 1) return FA_ERR_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+        return FA_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(total) * H * D * 2, nl = static_cast<size_t>(total) * H * 4;
+    const Range ins[7] = {range_of(q, n),   range_of(k, n),   range_of(v, n),
+                          range_of(o, n),   range_of(dO, n),  range_of(lse, nl),
+                          range_of(cu_seqlens, static_cast<size_t>(n_seq + 1) * 4)};
+    const Range outs[3] = {range_of(dq, n), range_of(dk, n), range_of(dv, n)};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 7; ++b)
+            if (overlap(outs[a], ins[b])) return FA_ERR_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlap(outs[a], outs[b])) return FA_ERR_ARG;
+    }
+    int dev = 0, sms = 0;
+    int rc = current_device(&dev, &sms);
+    if (rc != FA_OK) return rc;
+    return fa::launch_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, n_seq, max_seqlen, total, H, D, scale,
+                                 causal != 0, static_cast<cudaStream_t>(stream), knobs(), sms);
+}
+
 int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Tq, int Tk, int D,
               float scale, void* stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;

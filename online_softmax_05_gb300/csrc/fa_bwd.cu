@@ -181,7 +181,36 @@ struct BwdParams {
     float sl2, sl2_eff;
     int prescale;
     unsigned long long timeout_ns;
+    // Packed variable-length batch (VARLEN kernels): sequence s occupies rows
+    // cu_seqlens[s] .. cu_seqlens[s+1]-1 of the (total, H, D) tensors; T above
+    // is then the longest length the caller promises, and a "head" index bh
+    // of the grids is h * n_seq + s (per-row vectors: bh * T_pad + t).
+    const int* cu_seqlens;
+    int n_seq, total;
 };
+
+// Sequence of grid row bh: its length and first packed row (VARLEN), or the
+// dense T and row 0.  A sequence longer than T, or outside the packed rows,
+// is reported (FA_ERR_SEQLEN) and treated as empty by every role alike.
+struct SeqSpan {
+    int T, row0, head;
+};
+template <bool VARLEN>
+__device__ __forceinline__ SeqSpan seq_span(const BwdParams& p, int bh) {
+    if constexpr (!VARLEN) {
+        return SeqSpan{p.T, 0, bh};
+    } else {
+        const int sq = bh % p.n_seq;
+        SeqSpan r{0, p.cu_seqlens[sq], bh / p.n_seq};
+        r.T = p.cu_seqlens[sq + 1] - r.row0;
+        if (r.T < 0 || r.T > p.T || r.row0 < 0 || r.row0 + r.T > p.total) {
+            atomicCAS(&g_status_bwd, 0, kStatusBadSeqlen);
+            r.T = 0;
+            r.row0 = 0;
+        }
+        return r;
+    }
+}
 
 struct Ctl {
     volatile int* abort;
@@ -234,27 +263,38 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, Ctl c) {
 // D_i = rowsum(dO o O) ("Lab 06", section 4) and LSE2 = LSE * log2(e), both
 // stored NEGATED (the main kernels add them with FMAs); rows t >= T of the
 // padded vectors are 0.  8 elements per thread.
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          const float* __restrict__ lse, float* __restrict__ dvec,
                                                          float* __restrict__ lse2, int BH, int T, int T_pad,
-                                                         int* __restrict__ dq_next) {
+                                                         int* __restrict__ dq_next, const int* __restrict__ cu_seqlens,
+                                                         int n_seq, int H, int total) {
     constexpr int TPR = D / 8;            // threads per row
-    if (blockIdx.x == 0 && threadIdx.x == 0) *dq_next = 0;  // the dQ kernel's item counter
     constexpr int RPW = 32 / TPR;         // rows per warp
-    const long long total = static_cast<long long>(BH) * T_pad;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *dq_next = 0;  // the dQ kernel's item counter
+    const long long rows = static_cast<long long>(BH) * T_pad;
     const int lane = threadIdx.x & 31, sub = lane % TPR;
     const long long n_warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
     // warp-uniform loop: every lane reaches the shuffles below
-    for (long long wr = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; wr * RPW < total;
+    for (long long wr = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; wr * RPW < rows;
          wr += n_warps) {
         const long long r = wr * RPW + lane / TPR;
-        const bool in = r < total;
+        const bool in = r < rows;
         const int bh = in ? static_cast<int>(r / T_pad) : 0, t = in ? static_cast<int>(r % T_pad) : T_pad;
+        // this row's place in O / dO and in LSE; rows t >= len are padding
+        int len = T;
+        size_t orow = static_cast<size_t>(bh) * T + t, lrow = orow;
+        if constexpr (VARLEN) {
+            const int sq = bh % n_seq, h = bh / n_seq, row0 = cu_seqlens[sq];
+            len = cu_seqlens[sq + 1] - row0;
+            if (len < 0 || len > T || row0 < 0 || row0 + len > total) len = 0;  // reported by the main kernels
+            orow = static_cast<size_t>(row0 + t) * H + h;
+            lrow = static_cast<size_t>(h) * total + row0 + t;
+        }
         float acc = 0.f;
-        if (in && t < T) {
-            const size_t off = (static_cast<size_t>(bh) * T + t) * D + sub * 8;
+        if (in && t < len) {
+            const size_t off = orow * D + sub * 8;
             const uint4 a = *reinterpret_cast<const uint4*>(o + off);
             const uint4 b = *reinterpret_cast<const uint4*>(dO + off);
             const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -271,13 +311,13 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
         for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, TPR);
         if (in && sub == 0) {
             dvec[r] = -acc;
-            lse2[r] = (t < T) ? -lse[static_cast<size_t>(bh) * T + t] * kLog2e : 0.f;
+            lse2[r] = (t < len) ? -lse[lrow] * kLog2e : 0.f;
         }
     }
 }
 
 // ---------------------------------------------------------------- dK / dV kernel
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -323,7 +363,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const Ctl ctl{abort_flag, p.timeout_ns};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int T = p.T;
     // The dQ grid needs nothing from this one: it may launch as soon as every
     // CTA of this grid has started (its CTAs then fill SMs freed in the tail).
     griddep_launch_dependents();
@@ -336,6 +375,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // group in TMEM.
     const int bh = p.kt_major ? static_cast<int>(blockIdx.x % p.BH) : static_cast<int>(blockIdx.x / p.n_kt);
     const int kt = p.kt_major ? static_cast<int>(blockIdx.x / p.BH) : static_cast<int>(blockIdx.x % p.n_kt);
+    // the sequence of this row of the grid (packed batches: its own length and rows)
+    const SeqSpan span = seq_span<VARLEN>(p, bh);
+    const int T = span.T;
+    if (kt * kBN >= T) return;  // a shorter sequence has fewer key tiles: the whole CTA leaves
+    // TMA coordinates (y, z) of the 128-row tile starting at row r0 of grid row bhx
+    auto tile_yz = [&](int r0, int bhx, int& y, int& z) {
+        if constexpr (VARLEN) {
+            y = span.head;  // packed (total, H, D): (D, H, rows)
+            z = span.row0 + r0;
+        } else {
+            y = r0;
+            z = bhx;
+        }
+    };
     const int q_begin = bwd_q_begin(T, CAUSAL, kt, BM), q_end = bwd_q_end(T, BM);
     const int n_q = q_end - q_begin;
     const int n_it = n_q * p.group;
@@ -380,9 +433,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
             mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
+            int ky, kz;
+            tile_yz(kt * kBN, bh, ky, kz);
             for (int a = 0; a < C::kAtomsD; ++a) {
-                tma_load_3d_hint(sK + a * 128 * 128, &tm_k, kv_full, 64 * a, kt * kBN, bh, pol_kv);
-                tma_load_3d_hint(sV + a * 128 * 128, &tm_v, kv_full, 64 * a, kt * kBN, bh, pol_kv);
+                tma_load_3d_hint(sK + a * 128 * 128, &tm_k, kv_full, 64 * a, ky, kz, pol_kv);
+                tma_load_3d_hint(sV + a * 128 * 128, &tm_v, kv_full, 64 * a, ky, kz, pol_kv);
             }
             for (int it = 0; it < n_it; ++it) {
                 const int qt = q_tile_of(it), bhq = q_head_of(it);
@@ -392,8 +447,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const uint32_t fb = q_full(st);
                     mbar_arrive_expect_tx(fb, C::kQBytes + 2 * BM * 4);
                     ++q_armed;
+                    int qy, qz;
+                    tile_yz(qt * BM, bhq, qy, qz);
                     for (int a = 0; a < C::kAtomsD; ++a)
-                        tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qt * BM, bhq, pol_q);
+                        tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qy, qz, pol_q);
                     const size_t voff = static_cast<size_t>(bhq) * p.T_pad + static_cast<size_t>(qt) * BM;
                     bulk_load_1d(sLse(st), p.lse2 + voff, BM * 4, fb);
                     bulk_load_1d(sDv(st), p.dvec + voff, BM * 4, fb);
@@ -404,8 +461,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const uint32_t fb = do_full(st);
                     mbar_arrive_expect_tx(fb, C::kQBytes);
                     ++do_armed;
+                    int qy, qz;
+                    tile_yz(qt * BM, bhq, qy, qz);
                     for (int a = 0; a < C::kAtomsD; ++a)
-                        tma_load_3d_hint(sdO(st) + a * BM * 128, &tm_do, fb, 64 * a, qt * BM, bhq, pol_q);
+                        tma_load_3d_hint(sdO(st) + a * BM * 128, &tm_do, fb, 64 * a, qy, qz, pol_q);
                 }
             }
             // drain: copies still in flight must land before the CTA exits
@@ -633,7 +692,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // layout of the tensor maps (dK in Q ring stage 0, dV in dO ring stage 0:
         // every MMA has completed, so nothing reads them any more) and one
         // thread writes it out with TMA stores, which clip rows past T.
-        if (ok && warp_wait(dkv_full, 0, ctl)) {
+        if (VARLEN && ok && warp_wait(dkv_full, 0, ctl)) {
+            // packed rows past this sequence's end belong to the next one: row by row
+            tc_fence_after();
+            const int key = kt * kBN + 32 * wq + lane;  // 32x32b shape: this thread's own lane
+            const uint32_t col = h ? C::kDV : C::kDK;
+            const float mul = h ? 1.f : p.scale;
+            __nv_bfloat16* out = (h ? p.dv : p.dk) + (static_cast<size_t>(span.row0 + key) * p.Hq + span.head) * D;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + col + 32 * ch, v);
+                tmem_ld_wait();
+                reg_fence32(v);
+                if (key < T) {
+                    uint4* dst = reinterpret_cast<uint4*>(out + 32 * ch);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]) * mul, __uint_as_float(v[8 * g + 1]) * mul);
+                        w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]) * mul, __uint_as_float(v[8 * g + 3]) * mul);
+                        w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]) * mul, __uint_as_float(v[8 * g + 5]) * mul);
+                        w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]) * mul, __uint_as_float(v[8 * g + 7]) * mul);
+                        dst[g] = w;
+                    }
+                }
+            }
+        } else if (!VARLEN && ok && warp_wait(dkv_full, 0, ctl)) {
             tc_fence_after();
             const uint32_t row = 32u * wq + lane;  // 32x32b shape: this thread's own lane (key row)
             const uint32_t col = h ? C::kDV : C::kDK;
@@ -700,7 +785,7 @@ __device__ __forceinline__ void dq_item_at(int w, const BwdParams& p, int& bh, i
 }
 constexpr int kDqItemRing = 4;  // item numbers passed from the producer to the other roles
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -748,14 +833,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int T = p.T;
     struct Item {
         int bh, qt, bh_kv, n;
+        int T, row0, head;  // its sequence: length, first packed row, head (VARLEN)
     };
     auto item = [&](int bh, int qt) {
         Item it;
         it.bh = bh;
         it.qt = qt;
         it.bh_kv = (it.bh / p.Hq) * p.Hkv + (it.bh % p.Hq) / p.group;
-        it.n = fwd_num_kv_tiles(T, CAUSAL, it.qt);  // key tiles this query tile sees
+        const SeqSpan span = seq_span<VARLEN>(p, bh);
+        it.T = span.T;
+        it.row0 = span.row0;
+        it.head = span.head;
+        it.n = it.qt * 128 < it.T ? fwd_num_kv_tiles(it.T, CAUSAL, it.qt) : 0;  // key tiles this query tile sees
         return it;
+    };
+    // TMA coordinates (y, z) of the 128-row tile starting at row r0 of grid row bhx of item it
+    auto tile_yz = [&](const Item& it, int r0, int bhx, int& y, int& z) {
+        if constexpr (VARLEN) {
+            y = it.head;  // packed (total, H, D): (D, H, rows)
+            z = it.row0 + r0;
+        } else {
+            y = r0;
+            z = bhx;
+        }
     };
 
     if (tid == 0) {
@@ -803,19 +903,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // last item tells the other roles to stop)
                 const int slot = k % kDqItemRing;
                 if (!wait_bar(item_empty(slot), ((k / kDqItemRing) & 1) ^ 1, ctl)) break;
-                const int w = atomicAdd(p.dq_next, 1);
+                // (query tiles past a shorter sequence's end are skipped here, so
+                // the other roles only see items with work)
+                int w;
+                Item it;
+                while (true) {
+                    w = atomicAdd(p.dq_next, 1);
+                    if (w >= p.n_items) break;
+                    int w_bh, w_qt;
+                    dq_item_at<CAUSAL>(w, p, w_bh, w_qt);
+                    it = item(w_bh, w_qt);
+                    if (it.n > 0) break;
+                }
                 item_ring[slot] = w;
                 mbar_arrive(item_full(slot));
                 if (w >= p.n_items) break;
-                int w_bh, w_qt;
-                dq_item_at<CAUSAL>(w, p, w_bh, w_qt);
-                const Item it = item(w_bh, w_qt);
                 if (!wait_bar(qdo_empty, (qf & 1) ^ 1, ctl)) break;
                 mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
                 ++qf;
+                int qy, qz;
+                tile_yz(it, it.qt * 128, it.bh, qy, qz);
                 for (int a = 0; a < C::kAtomsD; ++a) {
-                    tma_load_3d_hint(sQ + a * 128 * 128, &tm_q, qdo_full, 64 * a, it.qt * 128, it.bh, pol_q);
-                    tma_load_3d_hint(sdO + a * 128 * 128, &tm_do, qdo_full, 64 * a, it.qt * 128, it.bh, pol_q);
+                    tma_load_3d_hint(sQ + a * 128 * 128, &tm_q, qdo_full, 64 * a, qy, qz, pol_q);
+                    tma_load_3d_hint(sdO + a * 128 * 128, &tm_do, qdo_full, 64 * a, qy, qz, pol_q);
                 }
                 bool fail = false;
                 for (int j = 0; j < it.n; ++j) {
@@ -827,9 +937,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         mbar_arrive_expect_tx(k_full(st), C::kTileBytes);
                         ++kf;
+                        int ky, kz;
+                        tile_yz(it, j * kBN, it.bh_kv, ky, kz);
                         for (int a = 0; a < C::kAtomsD; ++a)
-                            tma_load_3d_hint(sK(st) + a * 128 * 128, &tm_k, k_full(st), 64 * a, j * kBN, it.bh_kv,
-                                             pol_kv);
+                            tma_load_3d_hint(sK(st) + a * 128 * 128, &tm_k, k_full(st), 64 * a, ky, kz, pol_kv);
                     }
                     {
                         const int st = vf % NVS;
@@ -839,9 +950,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         mbar_arrive_expect_tx(v_full(st), C::kTileBytes);
                         ++vf;
+                        int vy, vz;
+                        tile_yz(it, j * kBN, it.bh_kv, vy, vz);
                         for (int a = 0; a < C::kAtomsD; ++a)
-                            tma_load_3d_hint(sV(st) + a * 128 * 128, &tm_v, v_full(st), 64 * a, j * kBN, it.bh_kv,
-                                             pol_kv);
+                            tma_load_3d_hint(sV(st) + a * 128 * 128, &tm_v, v_full(st), 64 * a, vy, vz, pol_kv);
                     }
                 }
                 if (fail) break;
@@ -980,7 +1092,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t nlse2 = f2(nlse, nlse), nd2 = f2(nd, nd);
             for (int j = 0; j < it.n; ++j) {
                 const uint32_t g = sc + j, b = g & 1;
-                const bool masked = bwd_tile_class(T, CAUSAL, 128, it.qt, j) == kMasked;
+                const bool masked = bwd_tile_class(it.T, CAUSAL, 128, it.qt, j) == kMasked;
                 if (!warp_wait<kCritSleep>(s_full(b), (g >> 1) & 1, ctl)) goto compute_done;
                 if (warp == 0 && lane == 0) FA_TRACE_EVENT(15, j);
                 tc_fence_after();
@@ -1007,7 +1119,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int key0 = j * kBN + 64 * h;
 #pragma unroll
                     for (int e = 0; e < 64; ++e)
-                        if (!bwd_elem_visible(T, CAUSAL, q, key0 + e)) pf[e] = 0.f;
+                        if (!bwd_elem_visible(it.T, CAUSAL, q, key0 + e)) pf[e] = 0.f;
                 }
                 if (!warp_wait<kCritSleep>(dp_full, (vc + j) & 1, ctl)) goto compute_done;
                 if (warp == 0 && lane == 0) FA_TRACE_EVENT(16, j);
@@ -1053,8 +1165,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dq_empty);
-                if (q < T) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.dq + (static_cast<size_t>(it.bh) * T + q) * D + h * kCols);
+                if (q < it.T) {
+                    const size_t drow = VARLEN ? static_cast<size_t>(it.row0 + q) * p.Hq + it.head
+                                               : static_cast<size_t>(it.bh) * T + q;
+                    uint4* dst = reinterpret_cast<uint4*>(p.dq + drow * D + h * kCols);
 #pragma unroll
                     for (int g = 0; g < kCols / 8; ++g) {
                         uint4 o;
@@ -1093,13 +1207,13 @@ bool set_smem_once(K kern, int bytes, bool& done) {
     return true;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                   const CUtensorMap& tdk, const CUtensorMap& tdv, BwdParams p, int BHq, int BHkv, cudaStream_t st,
                   const DebugKnobs& dbg, int num_sms) {
     static bool attr_a = false, attr_b = false;
-    auto ka = fa_bwd_dkdv_kernel<D, CAUSAL>;
-    auto kb = fa_bwd_dq_kernel<D, CAUSAL>;
+    auto ka = fa_bwd_dkdv_kernel<D, CAUSAL, VARLEN>;
+    auto kb = fa_bwd_dq_kernel<D, CAUSAL, VARLEN>;
     if (!set_smem_once(ka, DkvCfg<D>::kSmemBytes, attr_a) || !set_smem_once(kb, DqCfg<D>::kSmemBytes, attr_b))
         return -5;
     if (dbg.ev[2]) cudaEventRecord(dbg.ev[2], st);
@@ -1155,13 +1269,13 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     const long long blocks = (rows * (D / 8) + 255) / 256;
     const int pre_grid = static_cast<int>(blocks < 8LL * num_sms ? blocks : 8LL * num_sms);
     if (D == 64)
-        fa_bwd_pre_kernel<64><<<pre_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
-                                                            static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2,
-                                                            BH, T, T_pad, dq_next);
+        fa_bwd_pre_kernel<64, false><<<pre_grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2, BH, T, T_pad,
+            dq_next, nullptr, 1, Hq, 0);
     else
-        fa_bwd_pre_kernel<128><<<pre_grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
-                                                             static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2,
-                                                             BH, T, T_pad, dq_next);
+        fa_bwd_pre_kernel<128, false><<<pre_grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2, BH, T, T_pad,
+            dq_next, nullptr, 1, Hq, 0);
     if (cudaGetLastError() != cudaSuccess) return -5;
     BwdParams p;
     p.lse2 = lse2;
@@ -1184,11 +1298,76 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     p.prescale = p.sl2 > 0.f ? 0 : 1;
     p.sl2_eff = p.prescale ? 1.f : p.sl2;
     p.timeout_ns = dbg.timeout_ns;
+    p.cu_seqlens = nullptr;
+    p.n_seq = 1;
+    p.total = 0;
     if (D == 64)
-        return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms)
-                      : launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms);
-    return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms)
-                  : launch_main_t<128, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms);
+        return causal ? launch_main_t<64, true, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms)
+                      : launch_main_t<64, false, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms);
+    return causal ? launch_main_t<128, true, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms)
+                  : launch_main_t<128, false, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms);
+}
+
+// Packed variable-length backward: (total, H, D) tensors, sequences given by
+// cu_seqlens; the per-row vectors are laid out per (head, sequence) with
+// max_seqlen rounded up to 128 rows each.  ws as for run_bwd, sized by
+// bwd_varlen_scratch_bytes.
+int run_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, const int* cu_seqlens, int n_seq, int max_seqlen, int total, int H,
+                   int D, float scale, bool causal, void* ws, cudaStream_t stream, const DebugKnobs& dbg,
+                   int num_sms) {
+    const int BH = H * n_seq;
+    const int T_pad = cdiv(max_seqlen, 128) * 128;
+    const size_t bytes_vec = (static_cast<size_t>(BH) * T_pad * 4 + 255) / 256 * 256;
+    float* dvec = static_cast<float*>(ws);
+    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_vec);
+    int* dq_next = reinterpret_cast<int*>(static_cast<char*>(ws) + 2 * bytes_vec);
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_packed(&tq, q, total, H, D, 128) || !make_tmap_packed(&tk, k, total, H, D, 128) ||
+        !make_tmap_packed(&tv, v, total, H, D, 128) || !make_tmap_packed(&tdo, dO, total, H, D, 128))
+        return -5;
+    const long long rows = static_cast<long long>(BH) * T_pad;
+    const long long blocks = (rows * (D / 8) + 255) / 256;
+    const int pre_grid = static_cast<int>(blocks < 8LL * num_sms ? blocks : 8LL * num_sms);
+    if (D == 64)
+        fa_bwd_pre_kernel<64, true><<<pre_grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2, BH,
+            max_seqlen, T_pad, dq_next, cu_seqlens, n_seq, H, total);
+    else
+        fa_bwd_pre_kernel<128, true><<<pre_grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2, BH,
+            max_seqlen, T_pad, dq_next, cu_seqlens, n_seq, H, total);
+    if (cudaGetLastError() != cudaSuccess) return -5;
+    BwdParams p;
+    p.lse2 = lse2;
+    p.dvec = dvec;
+    p.dq_next = dq_next;
+    p.dq = static_cast<__nv_bfloat16*>(dq);
+    p.n_items = 0;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.T = max_seqlen;
+    p.T_pad = T_pad;
+    p.n_kt = cdiv(max_seqlen, kBN);
+    p.kt_major = 0;
+    p.BH = BH;
+    p.Hq = H;
+    p.Hkv = H;
+    p.group = 1;
+    p.scale = scale;
+    p.sl2 = scale * kLog2e;
+    p.prescale = p.sl2 > 0.f ? 0 : 1;
+    p.sl2_eff = p.prescale ? 1.f : p.sl2;
+    p.timeout_ns = dbg.timeout_ns;
+    p.cu_seqlens = cu_seqlens;
+    p.n_seq = n_seq;
+    p.total = total;
+    // dK and dV leave row by row (no TMA store), so their map arguments are placeholders
+    if (D == 64)
+        return causal ? launch_main_t<64, true, true>(tq, tk, tv, tdo, tq, tq, p, BH, BH, stream, dbg, num_sms)
+                      : launch_main_t<64, false, true>(tq, tk, tv, tdo, tq, tq, p, BH, BH, stream, dbg, num_sms);
+    return causal ? launch_main_t<128, true, true>(tq, tk, tv, tdo, tq, tq, p, BH, BH, stream, dbg, num_sms)
+                  : launch_main_t<128, false, true>(tq, tk, tv, tdo, tq, tq, p, BH, BH, stream, dbg, num_sms);
 }
 
 }  // namespace
@@ -1199,6 +1378,28 @@ size_t bwd_scratch_bytes(int B, int H, int T, int D) {
     const size_t T_pad = static_cast<size_t>(cdiv(T, 128)) * 128;
     const size_t bytes_vec = (BH * T_pad * 4 + 255) / 256 * 256;
     return 2 * bytes_vec + 256;  // + the dQ kernel's item counter
+}
+
+size_t bwd_varlen_scratch_bytes(int n_seq, int H, int max_seqlen) {
+    const size_t BH = static_cast<size_t>(n_seq) * H;
+    const size_t T_pad = static_cast<size_t>(cdiv(max_seqlen, 128)) * 128;
+    const size_t bytes_vec = (BH * T_pad * 4 + 255) / 256 * 256;
+    return 2 * bytes_vec + 256;
+}
+
+int launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, const int* cu_seqlens, int n_seq, int max_seqlen, int total,
+                      int H, int D, float scale, bool causal, cudaStream_t stream, const DebugKnobs& dbg,
+                      int num_sms) {
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bwd_varlen_scratch_bytes(n_seq, H, max_seqlen), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return -6;
+    }
+    int rc = run_bwd_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, n_seq, max_seqlen, total, H, D, scale,
+                            causal, ws, stream, dbg, num_sms);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == 0) rc = -5;
+    return rc;
 }
 
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,

@@ -29,6 +29,12 @@ int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, floa
                       int n_seq, int max_seqlen, int total, int H, int D, float scale, bool causal,
                       cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
 
+// Backward over a packed variable-length batch (the same layout; dq, dk, dv (total, H, D)).
+int launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, const int* cu_seqlens, int n_seq, int max_seqlen, int total,
+                      int H, int D, float scale, bool causal, cudaStream_t stream, const DebugKnobs& dbg,
+                      int num_sms);
+
 // Split-K decoding forward (fa_decode.cu).
 int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Tq, int Tk,
                   int D, float scale, cudaStream_t stream, int num_sms);

@@ -213,6 +213,24 @@ def attn_bwd_gqa(q, k, v, dout, scale: float, causal: bool):
     return dq, dk_r.reshape(B, Hkv, g, T, D).sum(axis=2), dv_r.reshape(B, Hkv, g, T, D).sum(axis=2), dvec
 
 
+def attn_bwd_varlen(q, k, v, dout, cu_seqlens, scale: float, causal: bool):
+    """Gradients of attn_fwd_varlen: q/k/v/dout [total, H, D].  By definition:
+    attn_bwd on each sequence's slice (no row of one sequence depends on
+    another's).  Returns (dQ, dK, dV), each [total, H, D]."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    total, H, D = q.shape
+    cu = [int(c) for c in np.asarray(cu_seqlens).ravel()]
+    dq, dk, dv = np.zeros((total, H, D)), np.zeros((total, H, D)), np.zeros((total, H, D))
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        if b <= a:
+            continue
+        t = lambda x: x[a:b].transpose(1, 0, 2)
+        g = attn_bwd(t(q), t(k), t(v), t(dout), scale, causal)
+        dq[a:b], dk[a:b], dv[a:b] = (x.transpose(1, 0, 2) for x in g[:3])
+    return dq, dk, dv
+
+
 def attn_fwd_varlen(q, k, v, cu_seqlens, scale: float, causal: bool):
     """Packed variable-length forward: q/k/v [total, H, D]; sequence s is rows
     cu_seqlens[s]:cu_seqlens[s+1] and attends only to itself, causal mask

@@ -138,3 +138,27 @@ def test_argument_errors_varlen(lib):
     assert f(cu=cu + 2) == -4
     assert f(q=base + 8) == -4
     assert f(o=k) == -8
+
+
+def test_argument_errors_bwd_varlen(lib):
+    base = 0x1000_0000
+    p = [base * (i + 1) for i in range(10)]   # q k v o dO lse dq dk dv cu
+
+    def f(**kw):
+        a = dict(zip("q k v o dO lse dq dk dv cu".split(), p))
+        a.update(kw)
+        return fa.fa_bwd_varlen(a["q"], a["k"], a["v"], a["o"], a["dO"], a["lse"], a["dq"], a["dk"], a["dv"], a["cu"],
+                                a.get("n_seq", 3), a.get("max_seqlen", 100), a.get("total", 250), 2, a.get("D", 128),
+                                a.get("scale", 0.1), a.get("causal", 0), None)
+    assert f(cu=None) == -1
+    assert f(dq=None) == -1
+    assert f(n_seq=0) == -2
+    assert f(max_seqlen=-1) == -2
+    assert f(total=0) == -2
+    assert f(D=96) == -3
+    assert f(cu=p[9] + 1) == -4
+    assert f(dk=p[7] + 8) == -4
+    assert f(causal=3) == -8
+    assert f(scale=float("nan")) == -8
+    assert f(dq=p[0]) == -8          # dq aliases q
+    assert f(dv=p[7]) == -8          # dv aliases dk

@@ -354,3 +354,35 @@ def test_varlen_matches_block_diagonal_softmax(causal):
         S = np.where(allowed, scale * q[:, h] @ k[:, h].T, -np.inf)
         np.testing.assert_allclose(o[:, h], scipy.special.softmax(S, axis=1) @ v[:, h], rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(lse[h], scipy.special.logsumexp(S, axis=1), rtol=1e-12, atol=1e-12)
+
+
+def test_varlen_backward_single_sequence_is_plain_backward():
+    q, k, v, do = (rng(60 + i).normal(size=(29, 2, 8)) for i in range(4))
+    g = oracle.attn_bwd_varlen(q, k, v, do, [0, 29], 0.5, True)
+    t = lambda x: x.transpose(1, 0, 2)
+    ref = oracle.attn_bwd(t(q), t(k), t(v), t(do), 0.5, True)
+    for a, b in zip(g, ref[:3]):
+        np.testing.assert_array_equal(a, t(b))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_matches_finite_differences(causal):
+    # L = sum(dO * O) over the whole packed batch, O from the (pinned) varlen
+    # forward; central differences of L against every input element
+    cu = np.array([0, 4, 4, 9, 10], dtype=np.int32)
+    total, H, D, scale, h = int(cu[-1]), 1, 3, 0.7, 1e-6
+    q, k, v, do = (rng(70 + i).normal(size=(total, H, D)) for i in range(4))
+    dq, dk, dv = oracle.attn_bwd_varlen(q, k, v, do, cu, scale, causal)
+
+    def loss(qq, kk, vv):
+        return float((oracle.attn_fwd_varlen(qq, kk, vv, cu, scale, causal)[0] * do).sum())
+
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(grad.shape):
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-7)

@@ -142,3 +142,125 @@ def test_serving_mix_sampled_rows(causal):
                                                   rows)
             assert o_ok(o[a + rows, h], o_ref), (s, h)
             assert np.abs(lse[h, a + rows] - lse_ref).max() <= LSE_TOL, (s, h)
+
+
+# ---------------------------------------------------------------- backward
+from tests.tolerances import grad_bound  # noqa: E402
+
+
+def run_bwd(q, k, v, do, cu, max_seqlen, causal, scale, expect_status=0):
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    cud = torch.from_numpy(cu).to(dev)
+    o, lse = fa.attention_forward_varlen(qd, kd, vd, cud, max_seqlen, causal=causal, scale=scale)
+    dq, dk, dv = (torch.zeros_like(qd) for _ in range(3))
+    total, H, D = q.shape
+    rc = fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cud, cu.size - 1, max_seqlen, total, H, D, scale,
+                          int(causal), torch.cuda.current_stream())
+    assert rc == 0, fa.fa_strerror(rc)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == expect_status
+    return tuple(to_f64(t.cpu()) for t in (dq, dk, dv))
+
+
+def packed4(lengths, H, D, seed, qk_std=1.0):
+    q, k, v, cu = packed(lengths, H, D, seed, qk_std)
+    g = torch.Generator().manual_seed(seed + 1000)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    return q, k, v, do, cu
+
+
+def check_grads(got, ref, rows=slice(None)):
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        bound = grad_bound(r[rows])
+        err = np.abs(g[rows] - r[rows]).max()
+        assert np.isfinite(g[rows]).all(), name
+        assert err <= bound, f"{name}: max err {err:.4g} > {bound:.4g}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mix", sorted(LENGTHS))
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_matches_oracle(mix, D, causal):
+    lengths = LENGTHS[mix]
+    q, k, v, do, cu = packed4(lengths, 3, D, seed=len(lengths) * 5 + D + int(causal))
+    scale = 1.0 / math.sqrt(D)
+    got = run_bwd(q, k, v, do, cu, max(lengths), causal, scale)
+    ref = oracle.attn_bwd_varlen(to_f64(q), to_f64(k), to_f64(v), to_f64(do), cu, scale, causal)
+    check_grads(got, ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_large_logits(causal):
+    lengths = [200, 385, 64]
+    q, k, v, do, cu = packed4(lengths, 2, 128, seed=12, qk_std=4.0)
+    scale = 1.0 / math.sqrt(128)
+    got = run_bwd(q, k, v, do, cu, 400, causal, scale)
+    ref = oracle.attn_bwd_varlen(to_f64(q), to_f64(k), to_f64(v), to_f64(do), cu, scale, causal)
+    check_grads(got, ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_single_sequence_equals_dense(causal):
+    T, H, D = 700, 4, 128
+    q, k, v, do, cu = packed4([T], H, D, seed=6)
+    got = run_bwd(q, k, v, do, cu, T, causal, 0.09)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.permute(1, 0, 2).contiguous().unsqueeze(0).to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=0.09)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=0.09)
+    torch.cuda.synchronize()
+    for g, d in zip(got, (dq, dk, dv)):
+        np.testing.assert_array_equal(g, to_f64(d[0].permute(1, 0, 2).cpu()))
+
+
+@pytest.mark.gpu
+def test_varlen_backward_sequence_longer_than_max_seqlen_is_reported():
+    # the second sequence (300 tokens) breaks the promised bound of 200: its
+    # gradients are left unwritten (zeros here) and FA_ERR_SEQLEN is recorded
+    lengths = [100, 300]
+    q, k, v, do, cu = packed4(lengths, 2, 64, seed=9)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    cud = torch.from_numpy(cu).to(dev)
+    # forward and backward with a bound that covers the first sequence only
+    o, lse = fa.attention_forward_varlen(qd, kd, vd, cud, 200, causal=True, scale=0.125)
+    assert fa.fa_get_device_status() == -11
+    dq, dk, dv = (torch.zeros_like(qd) for _ in range(3))
+    total, H, D = q.shape
+    assert fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cud, 2, 200, total, H, D, 0.125, 1,
+                            torch.cuda.current_stream()) == 0
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == -11
+    ref = oracle.attn_bwd_varlen(to_f64(q), to_f64(k), to_f64(v), to_f64(do), cu, 0.125, True)
+    got = tuple(to_f64(t.cpu()) for t in (dq, dk, dv))
+    check_grads(got, ref, rows=slice(0, 100))
+    for g in got:
+        assert not g[100:].any()
+    assert fa.fa_get_device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_serving_mix_sampled_rows(causal):
+    # 16 requests of 33..3000 tokens, 16 heads, D = 128; rows of dQ, dK and dV
+    # sampled per sequence and head against the oracle
+    rs = np.random.default_rng(19)
+    lengths = [int(x) for x in rs.integers(33, 3001, size=16)]
+    H, D = 16, 128
+    q, k, v, do, cu = packed4(lengths, H, D, seed=31)
+    scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = run_bwd(q, k, v, do, cu, max(lengths), causal, scale)
+    qf, kf, vf, dof = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
+    for s, L in enumerate(lengths):
+        a = int(cu[s])
+        rows = np.unique(np.concatenate([[0, L - 1], rs.integers(0, L, size=3)]))
+        for h in (0, (s * 7) % H, H - 1):
+            sl = slice(a, a + L)
+            rq, rk, rv, _, _ = oracle.attn_bwd_rows(qf[sl, h], kf[sl, h], vf[sl, h], dof[sl, h], scale, causal,
+                                                    rows, rows)
+            for name, g, r in (("dq", dq[a + rows, h], rq), ("dk", dk[a + rows, h], rk), ("dv", dv[a + rows, h], rv)):
+                assert np.abs(g - r).max() <= grad_bound(r), (name, s, h)
