@@ -67,7 +67,7 @@ def parse_args():
     ap.add_argument("--gqa", action="store_true",
                     help="grouped-query attention: B=2 Hq=16 Hkv=4 T=8192 D=128 causal, fwd and bwd TFLOP/s")
     ap.add_argument("--varlen", action="store_true",
-                    help="packed variable-length forward: 48 causal requests of 128..8192 tokens, H=16, D=128, "
+                    help="packed variable-length forward and backward: 48 causal requests of 128..8192 tokens, H=16, D=128, "
                          "against the same batch padded to the longest request")
     ap.add_argument("--configs", action="store_true",
                     help="every specified workload (fwd, bwd; the small forward also with a cold L2): one JSON line per case")
@@ -438,7 +438,7 @@ def run_gqa(args, B=2, Hq=16, Hkv=4, T=8192, D=128, causal=1):
 
 
 def run_varlen(args, n_seq=48, H=16, D=128, causal=1):
-    """fa_fwd_varlen throughput on a seeded serving mix, beside fa_fwd on the padded batch."""
+    """fa_fwd_varlen / fa_bwd_varlen throughput on a seeded serving mix, beside fa_fwd / fa_bwd on the padded batch."""
     import numpy as np
     import torch
     import online_softmax_05_gb300 as fa
@@ -449,18 +449,24 @@ def run_varlen(args, n_seq=48, H=16, D=128, causal=1):
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
     total, Tmax = int(cu[-1]), int(lengths.max())
     g = torch.Generator(device="cpu").manual_seed(0)
-    q, k, v = (torch.randn(total, H, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(3))
-    o = torch.empty_like(q)
+    q, k, v, do = (torch.randn(total, H, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(4))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
     lse = torch.empty(H, total, device=dev)
     cud = torch.from_numpy(cu).to(dev)
-    qp, kp, vp = (torch.zeros(n_seq, H, Tmax, D, dtype=torch.bfloat16, device=dev) for _ in range(3))
-    op = torch.empty_like(qp)
+    gd = torch.Generator(device=dev).manual_seed(1)
+    qp, kp, vp, dop = (torch.randn(n_seq, H, Tmax, D, generator=gd, device=dev).to(torch.bfloat16) for _ in range(4))
+    op, dqp, dkp, dvp = (torch.empty_like(qp) for _ in range(4))
     lp = torch.empty(n_seq, H, Tmax, device=dev)
     sc = D ** -0.5
-    f = lambda: fa.fa_fwd_varlen(q, k, v, o, lse, cud, n_seq, Tmax, total, H, D, sc, causal, stream)
-    fp = lambda: fa.fa_fwd(qp, kp, vp, op, lp, n_seq, H, Tmax, D, sc, causal, stream)
+    calls = {
+        "varlen": lambda: fa.fa_fwd_varlen(q, k, v, o, lse, cud, n_seq, Tmax, total, H, D, sc, causal, stream),
+        "padded": lambda: fa.fa_fwd(qp, kp, vp, op, lp, n_seq, H, Tmax, D, sc, causal, stream),
+        "varlen_bwd": lambda: fa.fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cud, n_seq, Tmax, total, H, D, sc,
+                                               causal, stream),
+        "padded_bwd": lambda: fa.fa_bwd(qp, kp, vp, op, dop, lp, dqp, dkp, dvp, n_seq, H, Tmax, D, sc, causal, stream),
+    }
     res = {}
-    for name, fn in (("varlen", f), ("padded", fp)):
+    for name, fn in calls.items():   # forwards first: each backward reads its forward's O and LSE
         for _ in range(max(3, args.warmup)):
             assert fn() == 0
         torch.cuda.synchronize(dev)
@@ -477,10 +483,15 @@ def run_varlen(args, n_seq=48, H=16, D=128, causal=1):
     useful = float(np.sum(4.0 * H * L * L * D / (2 if causal else 1)))
     peaks, src = load_peaks()
     tf = useful / res["varlen"] / 1e9
+    both = res["varlen"] + res["varlen_bwd"]
     print(json.dumps({"metric": "packed variable-length forward TFLOP/s (useful work)", "value": tf,
                       "unit": "TFLOP/s", "ms_per_call": res["varlen"], "padded_ms_per_call": res["padded"],
                       "padded_useful_tflops": useful / res["padded"] / 1e9, "speedup_vs_padded": res["padded"] / res["varlen"],
                       "frac_of_burst": tf / peaks["bf16_tflops"],
+                      "bwd_ms_per_call": res["varlen_bwd"], "bwd_useful_tflops": 2.5 * useful / res["varlen_bwd"] / 1e9,
+                      "padded_bwd_ms_per_call": res["padded_bwd"],
+                      "bwd_speedup_vs_padded": res["padded_bwd"] / res["varlen_bwd"],
+                      "fwd_bwd_useful_tflops": 3.5 * useful / both / 1e9,
                       "config": {"workload": f"varlen_n{n_seq}h{H}d{D}_len128to8192", "total_tokens": total,
                                  "max_seqlen": Tmax, "causal": bool(causal), "lengths": "uniform 128..8192, seed 0",
                                  "l2": "no flush: Q/K/V %.1f GB > 129 MB L2" % (3 * total * H * D * 2 / 1e9)},
