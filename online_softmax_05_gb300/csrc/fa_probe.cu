@@ -453,11 +453,16 @@ __global__ void __launch_bounds__(128, 1) probe_tmem_layout_kernel(uint32_t* ld_
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// Throughput of exp2: mode 0 = ex2.approx (MUFU), mode 1 = polynomial on
-// the FMA/ALU pipes (round-to-nearest by the 1.5*2^23 add, degree-3
-// least-squares fit of 2^f on [-1/2, 1/2], integer add into the exponent).
-// 8 independent chains per thread; cycles for `iters` x 8 evaluations per
-// thread are written to out[warp].
+// Throughput of the softmax's special-function work, 8 independent chains
+// per thread; cycles for `iters` rounds are written to out[warp]:
+//   mode 0  8 ex2.approx (MUFU) per round
+//   mode 1  8 exp2 as a polynomial on the FMA/ALU pipes (round-to-nearest by
+//           the 1.5*2^23 add, degree-3 least-squares fit of 2^f on
+//           [-1/2, 1/2], integer add into the exponent)
+//   mode 2  4 cvt.rn.bf16x2.f32 packs per round (each pair unpacked again
+//           by a mask, a shift and two adds, so the chains continue)
+//   mode 3  modes 0 and 2 interleaved: 8 ex2 and 4 packs per round, the
+//           softmax's mix (every P pair is exponentiated, then packed)
 __device__ __forceinline__ float exp2_poly3(float x) {
     x = fmaxf(x, -126.f);
     const float t = x + 12582912.f;  // 1.5 * 2^23: rounds x to an integer in the low mantissa bits
@@ -473,8 +478,19 @@ __global__ void probe_exp2_rate_kernel(int mode, int iters, float* sink, long lo
     __syncthreads();
     long long t0 = clock64();
     for (int i = 0; i < iters; ++i) {
+        if (mode <= 1) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) v[c] = (mode == 0 ? ex2_approx(v[c]) : exp2_poly3(v[c])) - 1.0f;
+            for (int c = 0; c < 8; ++c) v[c] = (mode == 0 ? ex2_approx(v[c]) : exp2_poly3(v[c])) - 1.0f;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float a = mode == 3 ? ex2_approx(v[2 * c]) : v[2 * c];
+                const float b = mode == 3 ? ex2_approx(v[2 * c + 1]) : v[2 * c + 1];
+                const uint32_t w = pack_bf16x2(a, b);
+                v[2 * c] = __uint_as_float(w & 0xffff0000u) - 1.0f;
+                v[2 * c + 1] = __uint_as_float(w << 16) - 1.0f;
+            }
+        }
     }
     long long t1 = clock64();
     float acc = 0.f;
@@ -492,7 +508,7 @@ extern "C" {
 int probe_exp2_rate(int mode, int iters, int warps, long long* out_host, float* max_rel_err) {
     float* sink = nullptr;
     long long* out = nullptr;
-    if (warps < 1 || warps > 32) return -1;
+    if (warps < 1 || warps > 32 || mode < 0 || mode > 3 || iters < 1 || iters > (1 << 20)) return -1;
     cudaMalloc(&sink, 1024 * sizeof(float));
     cudaMalloc(&out, 32 * sizeof(long long));
     fa::probe_exp2_rate_kernel<<<1, 32 * warps>>>(mode, iters, sink, out);

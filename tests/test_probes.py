@@ -138,6 +138,34 @@ def test_mma_sequence_report(plib, capsys):
     assert res[(1, 32, 0)] <= 1.3 * 64
 
 
+
+@pytest.mark.gpu
+def test_exp2_and_bf16_pack_rate_report(plib, capsys):
+    """Throughput on one SM (1 to 32 warps) of the softmax's special-function
+    work (see probe_exp2_rate_kernel): ex2.approx alone, exp2 as an FMA
+    polynomial, cvt.rn.bf16x2.f32 packs alone, and ex2 with packs in the
+    softmax's 2:1 mix.  Reported as operations per clock per SM; in the mixed
+    mode an ex2 and half a pack count as one step, so if the packs took no
+    issue or pipe time of their own it would match the ex2-alone rate."""
+    plib.probe_exp2_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong),
+                                     ctypes.c_void_p]
+    iters = 256
+    ops = {0: 8, 1: 8, 2: 4, 3: 8}   # counted operations per round per thread
+    names = {0: "ex2.approx", 1: "exp2 polynomial (FMA)", 2: "bf16x2 pack", 3: "ex2 + pack (2:1)"}
+    res = {}
+    for warps in (4, 8, 16, 32):
+        for mode in names:
+            o = (ctypes.c_longlong * 32)()
+            assert plib.probe_exp2_rate(mode, iters, warps, o, None) == 0
+            assert plib.probe_exp2_rate(mode, iters, warps, o, None) == 0
+            cyc = max(o[:warps])
+            res[(warps, mode)] = warps * 32 * iters * ops[mode] / cyc
+    with capsys.disabled():
+        print("\n  per SM and clock           4 warps  8 warps 16 warps 32 warps")
+        for mode, name in names.items():
+            print(f"  {name:24s}" + "".join(f"{res[(w, mode)]:9.1f}" for w in (4, 8, 16, 32)))
+    assert all(v > 0 for v in res.values())
+
 @pytest.mark.gpu
 def test_tmem_16x256b_load_and_16x128b_store_layout(plib):
     """tcgen05.ld.16x256b.x8: thread t, register j = 4k + i holds lane
