@@ -98,6 +98,7 @@ struct FwdParams {
     __nv_bfloat16* o_packed;  // O of the packed layout (stored row by row, not by TMA)
     int head_pairs;       // 1: the two query tiles of an item are two heads of one group at the same rows
     int n_tiles;          // query tiles per head
+    int single_tiles;     // 1: an item is one query tile (few items: each gets an SM of its own)
     float sl2_eff;  // multiplier applied inside exp2: scale*log2e, or 1 when prescaled
     float sl2;      // scale * log2(e)
     int prescale;   // 1 when scale <= 0: scores are multiplied by sl2 before the max
@@ -194,7 +195,15 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
         it.valid1 = it.tile[1] * kFwdBM < it.T;
         return it;
     }
-    if (p.head_pairs) {
+    if (p.single_tiles) {
+        // (query tile, head), heaviest tiles first; the second half is empty
+        const int t = p.n_tiles - 1 - w / p.BH, bh = w % p.BH;
+        it.tile[0] = t;
+        it.tile[1] = p.n_tiles;  // past T: the second warpgroup skips the item
+        it.bh[0] = it.bh[1] = bh;
+        it.bh_kv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
+        it.valid1 = false;
+    } else if (p.head_pairs) {
         const int per_t = p.BH / 2;  // head pairs over all batches
         const int t = p.n_tiles - 1 - w / per_t, rem = w % per_t;
         const int hp = rem % (p.Hq / 2), b = rem / (p.Hq / 2);
@@ -249,7 +258,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const Ctl ctl{abort_flag, p.timeout_ns};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int T = p.T;
 
     if (tid == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -699,6 +707,11 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     p.n_pairs = cdiv(T, 2 * kFwdBM);
     p.head_pairs = (p.group % 2 == 0) ? 1 : 0;
     p.n_items = p.head_pairs ? p.n_tiles * (BH / 2) : p.n_pairs * BH;
+    // Few items: give every query tile an SM of its own.  One tile's step
+    // (S, softmax, P V in sequence) is shorter than a pair's ping-pong step, and
+    // the SMs that pairs would leave idle do the other halves.
+    p.single_tiles = (2LL * p.n_items <= num_sms) ? 1 : 0;
+    if (p.single_tiles) p.n_items = p.n_tiles * BH;
     p.cu_seqlens = nullptr;
     p.n_seq = B;
     p.total = B * T;
@@ -735,6 +748,7 @@ int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, floa
     p.Hq = p.Hkv = H;
     p.group = 1;
     p.head_pairs = 0;
+    p.single_tiles = 0;
     p.n_tiles = cdiv(max_seqlen, kFwdBM);
     p.n_pairs = cdiv(max_seqlen, 2 * kFwdBM);
     p.n_items = p.n_pairs * n_seq * H;
