@@ -22,6 +22,7 @@ sample of the same workload, with the same metric and unit.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -40,7 +41,7 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd (bf16, 1×GB300) and % of dense BF16 p
 DEFAULT_WORKLOAD = "causal_b2h16t8192d128"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 DATASHEET_BF16_TFLOPS = 2250.0  # vendor dense bf16 figure per GPU, reported beside the measured peaks only
-CLOCK_FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
@@ -138,24 +139,31 @@ def recorded_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons (every 25 ms).  The
+    caller marks the timed region with mark(); the summary keeps the samples
+    taken inside it (all samples if none fell inside)."""
 
     def __init__(self, uuid: str | None):
         self.uuid = uuid
         self.proc = None
         self.path = None
+        self.marks = []
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                                          "--format=csv,noheader,nounits", "-lms", "25", "-f", self.path],
                                          stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
         return self
+
+    def mark(self):
+        """Host wall-clock time (local, as nvidia-smi stamps its samples)."""
+        self.marks.append(datetime.datetime.now())
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -165,28 +173,45 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    @staticmethod
+    def parse(lines, uuid=None, window=None):
+        """Rows of the sampler's CSV as a summary; window = (start, end) datetimes."""
         rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if uuid and uuid not in parts[1]:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if window and ts is not None and window[0] <= ts <= window[1]]
+        use = inside if inside else [r for _, r in rows]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "in_timed_region": 0}
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        sm = [float(r[2]) for r in use if num(r[2])]
+        smax = [float(r[3]) for r in use if num(r[3])]
+        power = [float(r[4]) for r in use if num(r[4])]
+        reasons = sorted({name for r in use for name, v in zip(REASON_NAMES, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(use), "in_timed_region": len(inside),
+                "power_w_max": max(power) if power else None,
+                "power_w_median": statistics.median(power) if power else None}
+
+    def summary(self):
+        lines = []
         try:
             with open(self.path) as f:
-                for line in f:
-                    parts = [p.strip() for p in line.split(",")]
-                    if len(parts) < 9:
-                        continue
-                    if self.uuid and self.uuid not in parts[0]:
-                        continue
-                    rows.append(parts)
+                lines = f.readlines()
             os.unlink(self.path)
         except Exception:
             pass
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
-        reasons = sorted({name for r in rows for name, v in zip(REASON_NAMES, r[5:9]) if v.lower() == "active"})
-        power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+        window = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else None
+        return self.parse(lines, self.uuid, window)
 
 
 _INPUT_CACHE = {}
@@ -585,11 +610,13 @@ def main():
     torch.cuda.synchronize(dev)
     lib.fa_set_timing_events(None, None, None, None, None)
     with ClockSampler(uuid) as clocks:
+        clocks.mark()
         t_start.record(stream)
         for s in range(K):
             step()
         t_end.record(stream)
         torch.cuda.synchronize(dev)
+        clocks.mark()
     if dist is not None:
         dist.barrier()
     status = fa.fa_get_device_status(stream)

@@ -126,3 +126,27 @@ def test_backward_head_pair_schedule_odd_tile_count():
         check(f"dq[{bh}]", dq[b, h, rows], rq)
         check(f"dk[{bh}]", dk[b, h, rows], rk)
         check(f"dv[{bh}]", dv[b, h, rows], rv)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_work_partition_does_not_change_bits_backward(D, causal):
+    # 4 heads of T = 2048 make few dK/dV CTAs, launched key tile major; 32 x 4
+    # heads make many, launched head by head; the dQ kernel hands its items out
+    # in whatever order CTAs ask.  Each key tile's dK / dV and each query tile's
+    # dQ are computed the same way wherever they run, so the shared heads'
+    # gradients must agree bit for bit.
+    B, H, T = 32, 4, 2048
+    q, k, v, do = make_inputs(B, H, T, D, seed=23)
+    dev = torch.device("cuda")
+    scale = D ** -0.5
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
+    big = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    small = fa.attention_backward(qd[:1].contiguous(), kd[:1].contiguous(), vd[:1].contiguous(), o[:1].contiguous(),
+                                  lse[:1].contiguous(), dod[:1].contiguous(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    for g_small, g_big in zip(small, big):
+        assert torch.equal(g_small[0], g_big[0])

@@ -112,6 +112,26 @@ def test_forward_workload_full_compare(name):
         assert np.abs(lse - lse_ref).max() <= LSE_TOL
 
 
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,T", [(64, 1024), (128, 2048), (128, 1000)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_work_partition_does_not_change_bits(D, T, causal):
+    # One batch of 4 heads has few work items, so each query tile gets an SM of
+    # its own; inside a batch of 16 x 8 heads the same heads are walked as pairs
+    # of query tiles by persistent CTAs.  Every row's arithmetic is the same in
+    # both, so the outputs of the shared heads must agree bit for bit.
+    H = 4
+    q, k, v, _ = make_inputs(16, H, T, D, seed=21)
+    dev = torch.device("cuda")
+    scale = D ** -0.5
+    o_small, l_small = fa.attention_forward(q[:1].to(dev), k[:1].to(dev), v[:1].to(dev), causal=causal, scale=scale)
+    o_big, l_big = fa.attention_forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    assert torch.equal(o_small[0], o_big[0])
+    assert torch.equal(l_small[0], l_big[0])
+
 def sample_rows(T, n_random, seed):
     rng = np.random.default_rng(seed)
     rows = set(range(min(T, 130))) | set(range(max(0, T - 130), T)) | set(rng.integers(0, T, n_random).tolist())
