@@ -5,7 +5,8 @@
 // "Output and saved state").
 //
 // One persistent CTA per SM walks work items (pair of 128-row query tiles,
-// batch*head).  Warp roles:
+// batch*head; a single query tile when there are too few pairs to fill half
+// the SMs).  Warp roles:
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one query row each)
 //   warps 4-7  softmax for query tile 1
 //   warp 8     TMA producer: Q tiles once per item, K/V tiles into a ring
