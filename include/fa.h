@@ -30,7 +30,12 @@
  * B*H*T_pad floats, T_pad = T rounded up to 128: D and log2-scaled LSE, plus
  * 256 bytes for a work counter)
  * stream-ordered with cudaMallocAsync on `stream` and releases it with
- * cudaFreeAsync on the same stream before returning.
+ * cudaFreeAsync on the same stream before returning.  Nothing on these paths
+ * synchronises, so every compute entry point may be called while `stream` is
+ * being captured into a CUDA graph (the workspace becomes allocation nodes,
+ * the backward's overlapped second kernel a programmatic dependency); a
+ * replay reads the input buffers as they are at replay time.
+ * fa_get_device_status synchronises and must not be captured.
  *
  * Errors.  Every entry point validates its arguments before launching
  * anything; on a validation error nothing is enqueued.  Return value 0
