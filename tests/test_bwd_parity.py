@@ -12,7 +12,7 @@ import torch
 import oracle
 import online_softmax_05_gb300 as fa
 from online_softmax_05_gb300.inputs import WORKLOADS, big_rows, make_inputs, to_f64, workload_inputs
-from tests.tolerances import grad_bound
+from tests.tolerances import LSE_TOL, grad_bound, o_ok
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -150,3 +150,30 @@ def test_work_partition_does_not_change_bits_backward(D, causal):
     assert fa.fa_get_device_status() == 0
     for g_small, g_big in zip(small, big):
         assert torch.equal(g_small[0], g_big[0])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
+def test_long_sequence_sampled_rows(D, causal):
+    # one head of 32731 tokens (256 tiles, the last one ragged): forward O and
+    # LSE and backward dQ, dK, dV on sampled rows, including both ends
+    T = 32768 - 37
+    q, k, v, do = make_inputs(1, 1, T, D, seed=41)
+    scale = D ** -0.5
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    rng = np.random.default_rng(43)
+    rows = sorted({0, 1, 127, 128, 16383, 16384, T - 129, T - 128, T - 2, T - 1} | set(rng.integers(0, T, 16).tolist()))
+    qf, kf, vf, df = (to_f64(t[0, 0]) for t in (q, k, v, do))
+    o_ref, lse_ref = oracle.attn_fwd_rows(qf, kf, vf, scale, causal, rows)
+    o_got = to_f64(o[0, 0].cpu())[rows]
+    assert o_ok(o_got, o_ref)
+    assert np.abs(lse[0, 0].cpu().double().numpy()[rows] - lse_ref).max() <= LSE_TOL
+    rq, rk, rv, _, _ = oracle.attn_bwd_rows(qf, kf, vf, df, scale, causal, rows, rows)
+    check("dq", to_f64(dq[0, 0].cpu())[rows], rq)
+    check("dk", to_f64(dk[0, 0].cpu())[rows], rk)
+    check("dv", to_f64(dv[0, 0].cpu())[rows], rv)
