@@ -13,7 +13,8 @@ import os
 import threading
 
 __all__ = ["fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen", "attention_forward_varlen", "fa_bwd_varlen", "attention_backward_varlen", "fa_decode", "attention_decode", "fa_bwd_noalloc", "fa_strerror", "fa_get_device_status", "fa_version",
-           "attention_forward", "attention_backward", "FAError", "library_path", "load_library"]
+           "attention_forward", "attention_backward", "FAError", "library_path", "load_library",
+           "FlashAttention", "flash_attention"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libfa.so")
@@ -275,3 +276,70 @@ def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float |
     if rc != FA_OK:
         raise FAError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------- autograd
+def _as_bhtd(t, name):
+    """(B, H, T, D) contiguous view of a (B, H, T, D) or (B, T, D) tensor."""
+    if t.dim() == 3:
+        t = t.unsqueeze(1)
+    elif t.dim() != 4:
+        raise ValueError(f"{name} must be (B, H, T, D) or (B, T, D)")
+    return t.contiguous()
+
+
+_autograd_cls = None
+
+
+def _make_autograd_class():
+    import torch
+
+    class FlashAttention(torch.autograd.Function):
+        """Exact attention as a differentiable op on the library's kernels.
+
+        Called as ``FlashAttention.apply(q, k, v, is_causal=False, scale=None)``,
+        the form of the public interface in "Flash Attention and Kernel
+        Optimization" ("Public Interface", "Autograd Wrapper and Backward
+        Path"), which the "Lab 06 - Attention kernels" work order also tests
+        end to end.  q, k, v: bf16 CUDA tensors (B, H, T, D), or (B, T, D) as
+        one head; scale defaults to 1/sqrt(D).  The forward runs fa_fwd and
+        saves O and LSE; the backward runs fa_bwd (the tiled backward kernels,
+        where that page rebuilds dense attention in PyTorch).
+        """
+
+        @staticmethod
+        def forward(ctx, q, k, v, is_causal=False, scale=None):
+            squeeze = q.dim() == 3
+            q4, k4, v4 = (_as_bhtd(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v")))
+            o, lse = attention_forward(q4, k4, v4, causal=bool(is_causal), scale=scale)
+            ctx.save_for_backward(q4, k4, v4, o, lse)
+            ctx.is_causal, ctx.scale, ctx.squeeze = bool(is_causal), scale, squeeze
+            return o.squeeze(1) if squeeze else o
+
+        @staticmethod
+        def backward(ctx, grad_o):
+            q4, k4, v4, o, lse = ctx.saved_tensors
+            do = _as_bhtd(grad_o, "grad of o")
+            dq, dk, dv = attention_backward(q4, k4, v4, o, lse, do, causal=ctx.is_causal, scale=ctx.scale)
+            if ctx.squeeze:
+                dq, dk, dv = dq.squeeze(1), dk.squeeze(1), dv.squeeze(1)
+            return dq, dk, dv, None, None
+
+    return FlashAttention
+
+
+def __getattr__(name):
+    # FlashAttention subclasses torch.autograd.Function; it is built on first
+    # use so that importing this module does not import torch
+    global _autograd_cls
+    if name == "FlashAttention":
+        with _lock:
+            if _autograd_cls is None:
+                _autograd_cls = _make_autograd_class()
+        return _autograd_cls
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
+
+
+def flash_attention(q, k, v, causal: bool = False, scale: float | None = None):
+    """O = softmax(q k^T * scale) v, differentiable (see FlashAttention)."""
+    return __getattr__("FlashAttention").apply(q, k, v, causal, scale)
