@@ -64,3 +64,35 @@ def test_noalloc_refuses_problems_larger_than_its_scratch(lib):
     rc = lib.fa_bwd_noalloc(*ptrs, 64, 32, 8192, 128, 0.088, 1, None)
     assert rc == -10
     assert "scratch" in fa.fa_strerror(rc)
+
+
+def test_noalloc_refuses_one_row_block_past_its_scratch():
+    # the scratch holds two (B*H, T_pad) float vectors plus 256 bytes: at
+    # T = 8192, 1024 heads need 64 MiB + 256 bytes and are refused before any
+    # device access (placeholder pointers; nothing is launched)
+    lib = fa.load_library()
+    base = 1 << 40
+    ptrs = [base * (i + 1) for i in range(9)]
+    assert lib.fa_bwd_noalloc(*ptrs, 1, 1024, 8192, 64, 0.125, 1, None) == -10
+    assert lib.fa_bwd_noalloc(*ptrs, 2, 512, 8192 - 100, 64, 0.125, 0, None) == -10   # T_pad is still 8192
+
+
+@pytest.mark.gpu
+def test_noalloc_runs_the_largest_problem_that_fits(lib):
+    # 1023 heads at T = 8192 leave 64 MiB - 65280 bytes: the largest head count
+    # that fits; the result equals fa_bwd's, compared on a few heads
+    B, H, T, D = 1, 1023, 8192, 64
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(71)
+    q, k, v, do = (torch.randn(B, H, T, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(4))
+    o, lse = fa.attention_forward(q, k, v, causal=True)
+    ref = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    got = [torch.empty_like(q) for _ in range(3)]
+    rc = lib.fa_bwd_noalloc(*(t.data_ptr() for t in (q, k, v, o, do, lse, *got)), B, H, T, D, D ** -0.5, 1,
+                            torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, fa.fa_strerror(rc)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    for h in (0, 511, H - 1):
+        for a, b in zip(got, ref):
+            assert torch.equal(a[0, h], b[0, h])
