@@ -72,101 +72,6 @@ def test_tma_probe_swizzle_and_zero_fill(plib, D, row0, bh):
 
 
 @pytest.mark.gpu
-def test_mma_chain_length_report(plib, capsys):
-    """Cycles per 128xNx16 bf16 tcgen05.mma when n = 256 instructions run as
-    chains of `chain` instructions on one accumulator, alternating between two
-    accumulators chain by chain (the shape of the attention kernels' products:
-    a chain per product, K / 16 instructions long).  Checks the long chains
-    of the dense K-major form stream within 30 % of 8192 FLOP/clk."""
-    plib.probe_mma_chain.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                     ctypes.POINTER(ctypes.c_longlong)]
-    kinds = {0: "SS, A and B K-major", 1: "SS, A K-major, B MN-major", 2: "TS (A in TMEM), B MN-major"}
-    rows = []
-    for N in (64, 128):
-        for kind in kinds:
-            for chain in (1, 2, 4, 8, 16, 32):
-                o = (ctypes.c_longlong * 1)()
-                assert plib.probe_mma_chain(N, 256, chain, kind, o) == 0
-                assert plib.probe_mma_chain(N, 256, chain, kind, o) == 0
-                rows.append((N, kinds[kind], chain, o[0] / 256.0))
-    with capsys.disabled():
-        print("\n  N  form                          chain  cycles/MMA")
-        for N, name, chain, c in rows:
-            print(f"{N:4d}  {name:28s} {chain:6d} {c:10.1f}")
-    for N, name, chain, c in rows:
-        if N == 128 and name == kinds[0] and chain == 32:
-            assert c <= 1.3 * 64
-
-
-@pytest.mark.gpu
-def test_mma_sequence_report(plib, capsys):
-    """Cycles per 128x128x16 MMA for loops of three 8-instruction chains shaped
-    like the attention kernels' (see probe_mma_seq_kernel): plain, with a
-    commit after each chain, with commit + satisfied wait + fence, and the
-    dQ kernel's SS / TS / SS rotation; on one SM and on every SM at once.
-    Then the first and the fourth with pseudo-random operands instead of 1.0
-    everywhere, and the wait / fence pair taken apart: the wait alone, the
-    fence alone, and the wait issued before the last two MMAs of the
-    previous chain; then the loop run by the whole warp with elect.sync
-    choosing the issuing lane, and descriptor offsets known only at run
-    time (as the kernels' ring stages are); and the warp-wide dQ loop while
-    the other three warps stream TMEM loads or shared-memory loads."""
-    import torch
-    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    plib.probe_mma_seq.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong)]
-    names = {0: "3 accumulators, SS chains", 1: "+ commit after each chain",
-             2: "+ satisfied wait and fence", 3: "dQ loop: SS, TS, SS",
-             4: "3 accumulators, random operands", 7: "dQ loop, random operands",
-             2 | 8: "wait without fence", 2 | 16: "fence without wait",
-             2 | 24: "wait early, fence after chain", 3 | 24: "dQ loop, wait early",
-             2 | 32: "wait + fence, whole warp", 3 | 32: "dQ loop, whole warp",
-             2 | 64: "wait + fence, run-time offsets", 3 | 64: "dQ loop, run-time offsets",
-             2 | 96: "whole warp, run-time offsets", 3 | 96: "dQ loop, warp, run-time offsets",
-             3 | 120: "dQ loop, warp, rt off, early",
-             3 | 96 | 128: "dQ loop (warp) + TMEM loads", 3 | 96 | 256: "dQ loop (warp) + smem loads"}
-    res = {}
-    for ctas, n_iter in ((1, 32), (n_sm, 32), (n_sm, 2048)):
-        for mode in names:
-            o = (ctypes.c_longlong * ctas)()
-            assert plib.probe_mma_seq(mode, n_iter, ctas, o) == 0
-            assert plib.probe_mma_seq(mode, n_iter, ctas, o) == 0
-            res[(ctas, n_iter, mode)] = float(np.median(np.array(o[:])) / (n_iter * 24))
-    with capsys.disabled():
-        print(f"\n  loop                              1 SM   {n_sm} SMs  {n_sm} SMs x 2048 iterations")
-        for mode, name in names.items():
-            print(f"  {name:32s} {res[(1, 32, mode)]:6.1f} {res[(n_sm, 32, mode)]:8.1f} {res[(n_sm, 2048, mode)]:8.1f}")
-    assert res[(1, 32, 0)] <= 1.3 * 64
-
-
-
-@pytest.mark.gpu
-def test_exp2_and_bf16_pack_rate_report(plib, capsys):
-    """Throughput on one SM (1 to 32 warps) of the softmax's special-function
-    work (see probe_exp2_rate_kernel): ex2.approx alone, exp2 as an FMA
-    polynomial, cvt.rn.bf16x2.f32 packs alone, and ex2 with packs in the
-    softmax's 2:1 mix.  Reported as operations per clock per SM; in the mixed
-    mode an ex2 and half a pack count as one step, so if the packs took no
-    issue or pipe time of their own it would match the ex2-alone rate."""
-    plib.probe_exp2_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong),
-                                     ctypes.c_void_p]
-    iters = 256
-    ops = {0: 8, 1: 8, 2: 4, 3: 8}   # counted operations per round per thread
-    names = {0: "ex2.approx", 1: "exp2 polynomial (FMA)", 2: "bf16x2 pack", 3: "ex2 + pack (2:1)"}
-    res = {}
-    for warps in (4, 8, 16, 32):
-        for mode in names:
-            o = (ctypes.c_longlong * 32)()
-            assert plib.probe_exp2_rate(mode, iters, warps, o, None) == 0
-            assert plib.probe_exp2_rate(mode, iters, warps, o, None) == 0
-            cyc = max(o[:warps])
-            res[(warps, mode)] = warps * 32 * iters * ops[mode] / cyc
-    with capsys.disabled():
-        print("\n  per SM and clock           4 warps  8 warps 16 warps 32 warps")
-        for mode, name in names.items():
-            print(f"  {name:24s}" + "".join(f"{res[(w, mode)]:9.1f}" for w in (4, 8, 16, 32)))
-    assert all(v > 0 for v in res.values())
-
-@pytest.mark.gpu
 def test_tmem_16x256b_load_and_16x128b_store_layout(plib):
     """tcgen05.ld.16x256b.x8: thread t, register j = 4k + i holds lane
     t/4 (+8 for i >= 2), column 8k + 2 (t % 4) + (i % 2).
