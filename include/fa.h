@@ -62,7 +62,8 @@ typedef enum fa_status {
     FA_ERR_ARG = -8,             /* causal not 0/1, or scale not finite */
     FA_ERR_ARCH = -9,            /* current device is not compute capability 10.3 (sm_103a) */
     FA_ERR_SCRATCH = -10,        /* fa_bwd_noalloc: problem needs more than its fixed scratch buffer */
-    FA_ERR_SEQLEN = -11          /* recorded by a kernel: a cu_seqlens length is negative or above max_seqlen */
+    FA_ERR_SEQLEN = -11,         /* recorded by a kernel: a cu_seqlens length is negative or above max_seqlen */
+    FA_ERR_DEBUG_CHECK = -12     /* debug library only: a kernel's run-time index failed its bounds check */
 } fa_status;
 
 /*
@@ -111,8 +112,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  *   to a multiple of 128 (B*H*T_pad just under 8 M rows); larger problems
  *   return FA_ERR_SCRATCH and nothing is enqueued.
  * Set-up: the first call on each device looks up the buffer's device
- *   address (cudaGetSymbolAddress); make that first call before any stream
- *   capture.
+ *   address (cudaGetSymbolAddress) in the context current at that moment and
+ *   keeps it for the rest of the process; make that first call before any
+ *   stream capture.  The kept address belongs to that context: after
+ *   cudaDeviceReset, or from another (non-primary) context on the same
+ *   device, it is stale, so do not call fa_bwd_noalloc there.
  * Sharing: every call uses the same buffer, which keeps the previous call's
  *   contents (the backward rewrites all of it before reading it).  Calls whose
  *   work overlaps on the GPU (different streams, or different host threads
@@ -243,12 +247,27 @@ int fa_sched_tile_rows(int D, int* bm_fwd, int* bn, int* bm_bwd);
  * Test hooks (host state, read at the next launch; default off).
  * fa_debug_set_wait_timeout_ns: bound of every in-kernel wait (default 2 s).
  * fa_debug_inject: 0 = off; 1 = the forward's load warp skips its first
- *   K/V tile copy, so the kernel's bounded waits run out and it reports
- *   FA_ERR_DEVICE_TIMEOUT instead of hanging.  Used to test failure
- *   detection without faulting the GPU.
+ *   K/V tile copy; 2 = the load warp of the backward's first dK/dV CTA skips
+ *   its first Q tile copy; 3 = the load warp of the backward's first dQ CTA
+ *   skips its first K tile copy.  The waits that depend on the missing copy
+ *   run out, the CTA gives up (it waits, bounded, for its copies and MMAs in
+ *   flight, frees its tensor memory and exits) and FA_ERR_DEVICE_TIMEOUT is
+ *   reported instead of a hang; the outputs of that call are not valid.
+ *   Used to test failure detection without faulting the GPU.  Other values
+ *   return FA_ERR_ARG.
  */
 int fa_debug_set_wait_timeout_ns(unsigned long long ns);
 int fa_debug_inject(int mode);
+
+/*
+ * 1 in the debug build of the library (compiled with FA_DEBUG), 0 in the
+ * product build.  In the debug build every kernel checks the tile
+ * coordinates, ring stages, per-row vector offsets and tensor-memory columns
+ * it computes at run time before it uses them; a failed check skips the
+ * access, makes the CTA give up through its bounded-wait exit path, and is
+ * reported by fa_get_device_status as FA_ERR_DEBUG_CHECK.  Nothing traps.
+ */
+int fa_debug_checks_enabled(void);
 
 /*
  * Measurement hook (default off; host state read by each call).  When the

@@ -24,7 +24,8 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_SHAPE", -3: "FA_ERR_UNSUPPORTED", -4: "FA_ERR_ALIGN",
                 -5: "FA_ERR_CUDA", -6: "FA_ERR_NOMEM", -7: "FA_ERR_DEVICE_TIMEOUT", -8: "FA_ERR_ARG",
-                -9: "FA_ERR_ARCH", -10: "FA_ERR_SCRATCH", -11: "FA_ERR_SEQLEN"}
+                -9: "FA_ERR_ARCH", -10: "FA_ERR_SCRATCH", -11: "FA_ERR_SEQLEN",
+                -12: "FA_ERR_DEBUG_CHECK"}
 
 
 class FAError(RuntimeError):

@@ -1,7 +1,11 @@
 """Build the CUDA libraries in-tree with nvcc for sm_103a.
 
   libfa.so        the product: C-ABI entry points of include/fa.h
-  libfa_probe.so  test-only bring-up kernels (descriptor / TMA checks)
+  libfa_debug.so  the same sources built with -DFA_DEBUG: every kernel checks
+                  its run-time tile, ring-stage, vector and tensor-memory
+                  indices before use and reports FA_ERR_DEBUG_CHECK instead of
+                  touching memory out of bounds (tests only; slower)
+  libfa_probe.so  test-only bring-up kernels (descriptor / TMA / TMEM layout checks)
 
 Translation units compile in parallel; a unit is rebuilt only when its
 source or any header under csrc/ or include/ is newer than its object.
@@ -22,6 +26,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 
 LIB = os.path.join(PKG, "libfa.so")
+DEBUG_LIB = os.path.join(PKG, "libfa_debug.so")
 PROBE_LIB = os.path.join(PKG, "libfa_probe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -45,9 +50,11 @@ def _headers_mtime() -> float:
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def _compile(unit: str, extra: list[str], force: bool, verbose: bool) -> str:
+def _compile(unit: str, extra: list[str], force: bool, verbose: bool, debug: bool = False) -> str:
     src = os.path.join(CSRC, unit)
-    obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
+    obj = os.path.join(BUILD, unit.replace(".cu", ".debug.o" if debug else ".o"))
+    if debug:
+        extra = extra + ["-DFA_DEBUG"]
     if (not force and os.path.exists(obj)
             and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime())):
         return obj
@@ -76,17 +83,21 @@ def _link(objs: list[str], out: str, verbose: bool) -> None:
     os.replace(out + ".tmp", out)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, probes: bool = True) -> str:
-    """Compile every CUDA translation unit and link libfa.so (+ libfa_probe.so)."""
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, probes: bool = True,
+          debug: bool = True) -> str:
+    """Compile every CUDA translation unit and link libfa.so (+ libfa_debug.so, libfa_probe.so)."""
     os.makedirs(BUILD, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
-    units = PRODUCT_UNITS + (PROBE_UNITS if probes else [])
-    with cf.ThreadPoolExecutor(max_workers=len(units)) as ex:
-        futs = {u: ex.submit(_compile, u, extra, force, verbose or ptxas_verbose) for u in units}
-        objs = {u: f.result() for u, f in futs.items()}
-    _link([objs[u] for u in PRODUCT_UNITS], LIB, verbose)
+    jobs = [(u, False) for u in PRODUCT_UNITS] + [(u, False) for u in (PROBE_UNITS if probes else [])]
+    jobs += [(u, True) for u in (PRODUCT_UNITS if debug else [])]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        futs = {j: ex.submit(_compile, j[0], extra, force, verbose or ptxas_verbose, j[1]) for j in jobs}
+        objs = {j: f.result() for j, f in futs.items()}
+    _link([objs[(u, False)] for u in PRODUCT_UNITS], LIB, verbose)
+    if debug:
+        _link([objs[(u, True)] for u in PRODUCT_UNITS], DEBUG_LIB, verbose)
     if probes:
-        _link([objs[u] for u in PROBE_UNITS], PROBE_LIB, verbose)
+        _link([objs[(u, False)] for u in PROBE_UNITS], PROBE_LIB, verbose)
     return LIB
 
 

@@ -91,6 +91,7 @@ const char* fa_strerror(int status) {
         case FA_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
         case FA_ERR_SEQLEN: return "a cu_seqlens length is negative or above max_seqlen (recorded by the kernel)";
         case FA_ERR_SCRATCH: return "fa_bwd_noalloc: the problem needs more than the fixed 64 MiB scratch buffer";
+        case FA_ERR_DEBUG_CHECK: return "debug library: a kernel's run-time index failed its bounds check (access skipped)";
         default: return "unknown fa_status";
     }
 }
@@ -334,8 +335,16 @@ int fa_set_timing_events(void* fwd_begin, void* fwd_end, void* bwd_begin, void* 
     return FA_OK;
 }
 
+int fa_debug_checks_enabled(void) {
+#ifdef FA_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 int fa_debug_inject(int mode) {
-    if (mode < 0 || mode > 1) return FA_ERR_ARG;
+    if (mode < 0 || mode > 3) return FA_ERR_ARG;
     g_inject.store(mode);
     return FA_OK;
 }

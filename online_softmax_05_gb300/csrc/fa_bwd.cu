@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_check.cuh"
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 #include "fa_sched.h"
@@ -41,45 +42,7 @@ namespace fa {
 
 static __device__ int g_status_bwd;
 
-// Optional cycle tracing of one CTA's pipeline (build with -DFA_TRACE; off in
-// the library): slot = event kind, index = query-tile iteration.
-#ifdef FA_TRACE
-constexpr int kTraceSlots = 28, kTraceLen = 512;
-static __device__ unsigned long long g_trace[kTraceSlots][kTraceLen];
-#define FA_TRACE_EVENT(slot, idx)                                                  \
-    do {                                                                           \
-        if (blockIdx.x == 0 && (idx) < kTraceLen) g_trace[slot][idx] = clock64(); \
-    } while (0)
-// Per-CTA timeline: [kernel 0 = dK/dV, 1 = dQ][CTA][SM id, entry, end of MMA issue, exit], in
-// global-timer nanoseconds.
-__device__ __forceinline__ unsigned sm_id() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
-    return r;
-}
-constexpr int kCtaTraceMax = 8192;
-static __device__ unsigned long long g_cta_trace[2][kCtaTraceMax][4];
-#define FA_CTA_EVENT(kern, slot, value)                                               \
-    do {                                                                              \
-        if (blockIdx.x < kCtaTraceMax) g_cta_trace[kern][blockIdx.x][slot] = (value); \
-    } while (0)
-#else
-#define FA_TRACE_EVENT(slot, idx) \
-    do {                          \
-    } while (0)
-#define FA_CTA_EVENT(kern, slot, value) \
-    do {                                \
-    } while (0)
-#endif
-
 namespace {
-
-#ifndef FA_CRIT_SLEEP
-#define FA_CRIT_SLEEP 0
-#endif
-// Waits on the MMA <-> compute critical path poll back to back unless built
-// with FA_CRIT_SLEEP=1; every other wait lets the hardware park the thread.
-constexpr bool kCritSleep = FA_CRIT_SLEEP != 0;
 
 constexpr int kBwdThreads = 320;  // both main kernels: 8 compute warps, producer, MMA issuer
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -181,6 +144,8 @@ struct BwdParams {
     float sl2, sl2_eff;
     int prescale;
     unsigned long long timeout_ns;
+    int inject;           // test hook: 2 = the dK/dV grid's first CTA drops its first Q fill, 3 = the dQ
+                          // grid's first CTA drops its first K fill (its waits then run out)
     // Packed variable-length batch (VARLEN kernels): sequence s occupies rows
     // cu_seqlens[s] .. cu_seqlens[s+1]-1 of the (total, H, D) tensors; T above
     // is then the longest length the caller promises, and a "head" index bh
@@ -328,10 +293,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr int NQS = C::kQStages, NDS = C::kDOStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_window<C::kSlack>(smem_raw);
-    if (threadIdx.x == 0) {
-        FA_CTA_EVENT(0, 0, sm_id());
-        FA_CTA_EVENT(0, 1, globaltimer_ns());
-    }
     const uint32_t sbase = smem_u32(smem);
     if constexpr (C::kSlack == 0) {
         if (sbase & 1023u) {
@@ -430,12 +391,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t q_armed = 0, do_armed = 0;  // fills issued per ring
+            int q_skipped = -1;                  // Q fill the test hook dropped
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
-            mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
             int ky, kz;
             tile_yz(kt * kBN, bh, ky, kz);
-            for (int a = 0; a < C::kAtomsD; ++a) {
+            // the key tile starts inside its sequence and its head exists
+            const bool kv_ok = FA_CHECK(kt * kBN < T && bh >= 0 && bh < p.BH, &g_status_bwd, abort_flag);
+            if (kv_ok) mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
+            for (int a = 0; kv_ok && a < C::kAtomsD; ++a) {
                 tma_load_3d_hint(sK + a * 128 * 128, &tm_k, kv_full, 64 * a, ky, kz, pol_kv);
                 tma_load_3d_hint(sV + a * 128 * 128, &tm_v, kv_full, 64 * a, ky, kz, pol_kv);
             }
@@ -445,19 +409,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int st = it % NQS;
                     if (!wait_bar(q_empty(st), ((it / NQS) & 1) ^ 1, ctl)) break;
                     const uint32_t fb = q_full(st);
-                    mbar_arrive_expect_tx(fb, C::kQBytes + 2 * BM * 4);
-                    ++q_armed;
-                    int qy, qz;
-                    tile_yz(qt * BM, bhq, qy, qz);
-                    for (int a = 0; a < C::kAtomsD; ++a)
-                        tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qy, qz, pol_q);
                     const size_t voff = static_cast<size_t>(bhq) * p.T_pad + static_cast<size_t>(qt) * BM;
-                    bulk_load_1d(sLse(st), p.lse2 + voff, BM * 4, fb);
-                    bulk_load_1d(sDv(st), p.dvec + voff, BM * 4, fb);
+                    // the query tile and head exist, the stage lies inside the window and the
+                    // -LSE2 / -D slices inside their (B*Hq, T_pad) vectors
+                    if (!FA_CHECK(qt >= 0 && qt * BM < T && bhq >= 0 && bhq < p.BH * p.group && st < NQS &&
+                                      C::kQRingOff + (st + 1) * C::kQStageBytes <= C::kDORingOff &&
+                                      voff + BM <= static_cast<size_t>(p.BH) * p.group * p.T_pad,
+                                  &g_status_bwd, abort_flag))
+                        break;
+                    if (it == 0 && p.inject == 2 && blockIdx.x == 0) {  // test hook: never deliver this tile
+                        q_skipped = static_cast<int>(q_armed++);
+                    } else {
+                        mbar_arrive_expect_tx(fb, C::kQBytes + 2 * BM * 4);
+                        ++q_armed;
+                        int qy, qz;
+                        tile_yz(qt * BM, bhq, qy, qz);
+                        for (int a = 0; a < C::kAtomsD; ++a)
+                            tma_load_3d_hint(sQ(st) + a * BM * 128, &tm_q, fb, 64 * a, qy, qz, pol_q);
+                        bulk_load_1d(sLse(st), p.lse2 + voff, BM * 4, fb);
+                        bulk_load_1d(sDv(st), p.dvec + voff, BM * 4, fb);
+                    }
                 }
                 {   // dO tile
                     const int st = it % NDS;
                     if (!wait_bar(do_empty(st), ((it / NDS) & 1) ^ 1, ctl)) break;
+                    if (!FA_CHECK(st < NDS && C::kDORingOff + (st + 1) * C::kQBytes <= C::kBarOff, &g_status_bwd,
+                                  abort_flag))
+                        break;
                     const uint32_t fb = do_full(st);
                     mbar_arrive_expect_tx(fb, C::kQBytes);
                     ++do_armed;
@@ -470,9 +448,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // drain: copies still in flight must land before the CTA exits
             volatile int never = 0;
             Ctl drain{&never, 100000000ull};
-            wait_bar(kv_full, 0, drain);
+            if (kv_ok) wait_bar(kv_full, 0, drain);
             for (uint32_t f = q_armed > NQS ? q_armed - NQS : 0; f < q_armed; ++f)
-                wait_bar(q_full(f % NQS), (f / NQS) & 1, drain);
+                if (static_cast<int>(f) != q_skipped) wait_bar(q_full(f % NQS), (f / NQS) & 1, drain);
             for (uint32_t f = do_armed > NDS ? do_armed - NDS : 0; f < do_armed; ++f)
                 wait_bar(do_full(f % NDS), (f / NDS) & 1, drain);
         }
@@ -521,43 +499,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             issue_dp(0);
             for (int it = 0; it < n_it; ++it) {
                 const int qs = it % NQS, ds = it % NDS;
-                FA_TRACE_EVENT(0, it);
                 if (!wait_all(p_full, it & 1, ctl)) goto mma_teardown;
-                FA_TRACE_EVENT(1, it);
                 tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < NKV; ++s)
                     if (leader) mma_ts_d(tmem + C::kDV, tmem + C::kP + s * 8, dO_mn, ds * kDOStage16 + s * (2048 >> 4),
                              C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
                 if (leader) mma_commit(do_empty(ds));
-                FA_TRACE_EVENT(7, it);
                 if (it + 1 < n_it) {
                     if (!wait_all(q_full((it + 1) % NQS), ((it + 1) / NQS) & 1, ctl))
                         goto mma_teardown;
                     tc_fence_after();
                     issue_s((it + 1) % NQS);
                 }
-                FA_TRACE_EVENT(2, it);
                 if (!wait_all(ds_full, it & 1, ctl)) goto mma_teardown;
-                FA_TRACE_EVENT(10, it);
                 tc_fence_after();
 #pragma unroll
                 for (int s = 0; s < NKV; ++s)
                     if (leader) mma_ts_d(tmem + C::kDK, tmem + C::kDS + s * 8, dQ_mn, qs * kQStage16 + s * (2048 >> 4),
                              C::kIdescDKV, (it > 0 || s > 0) ? 1u : 0u);
                 if (leader) mma_commit(q_empty(qs));
-                FA_TRACE_EVENT(11, it);
                 if (it + 1 < n_it) {
                     const int ds1 = (it + 1) % NDS;
                     if (!wait_all(do_full(ds1), ((it + 1) / NDS) & 1, ctl)) goto mma_teardown;
                     tc_fence_after();
                     issue_dp(ds1);
-                    FA_TRACE_EVENT(8, it);
                 }
             }
             if (leader) mma_commit(dkv_full);
         mma_teardown:
-            FA_CTA_EVENT(0, 2, globaltimer_ns());
             if (leader) {
                 mma_commit(mma_done);
                 volatile int never = 0;
@@ -586,11 +556,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int st = it % NQS;
             const int qt = q_tile_of(it), q0 = qt * BM;
             const bool masked = bwd_tile_class(T, CAUSAL, BM, qt, kt) == kMasked;
-            if (!warp_wait(q_full(st), (it / NQS) & 1, ctl) || !warp_wait<kCritSleep>(s_full, it & 1, ctl)) {
+            if (!warp_wait(q_full(st), (it / NQS) & 1, ctl) || !warp_wait<false>(s_full, it & 1, ctl)) {
                 ok = false;
                 break;
             }
-            if (warp == 0 && lane == 0) FA_TRACE_EVENT(3, it);
             tc_fence_after();
             // this thread's 16 query columns: 64h + 8k + 2 t4 + {0, 1}
             const float2* lse2v = reinterpret_cast<const float2*>(smem + (sLse(st) - sbase)) + 32 * h + t4;
@@ -649,12 +618,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
-            if (warp == 0 && lane == 0) FA_TRACE_EVENT(4, it);
-            if (!warp_wait<kCritSleep>(dp_full, it & 1, ctl)) {
+            if (!warp_wait<false>(dp_full, it & 1, ctl)) {
                 ok = false;
                 break;
             }
-            if (warp == 0 && lane == 0) FA_TRACE_EVENT(5, it);
             tc_fence_after();
             uint32_t dr[64];
             tmem_ld_16x256b_x8(lane_base + C::kDP + 64 * h, dr);
@@ -685,7 +652,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
-            if (warp == 0 && lane == 0) FA_TRACE_EVENT(6, it);
         }
         // epilogue: warpgroup 0 stores dK * scale, warpgroup 1 stores dV.  Each
         // stages its 128 x D bf16 tile in shared memory in the 128-byte swizzled
@@ -744,7 +710,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(epi_bar(h));
-            if (wq == 0 && lane == 0 && wait_bar(epi_bar(h), 0, ctl)) {
+            if (wq == 0 && lane == 0 && wait_bar(epi_bar(h), 0, ctl) &&
+                FA_CHECK(kt * kBN < T && bh >= 0 && bh < p.BH, &g_status_bwd, abort_flag)) {
                 for (int a = 0; a < C::kAtomsD; ++a)
                     tma_store_3d(h ? &tm_dv : &tm_dk, stage + a * (BM * 128), 64 * a, kt * kBN, bh);
                 bulk_commit();
@@ -758,7 +725,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
-        if (lane == 0) FA_CTA_EVENT(0, 3, globaltimer_ns());
     }
 }
 
@@ -794,10 +760,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr int NKS = C::kKStages, NVS = C::kVStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_window<C::kSlack>(smem_raw);
-    if (threadIdx.x == 0) {
-        FA_CTA_EVENT(1, 0, sm_id());
-        FA_CTA_EVENT(1, 1, globaltimer_ns());
-    }
     const uint32_t sbase = smem_u32(smem);
     if constexpr (C::kSlack == 0) {
         if (sbase & 1023u) {
@@ -896,6 +858,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t kf = 0, vf = 0, qf = 0;  // fills issued (K ring, V ring, Q/dO pair)
+            int k_skipped = -1;               // K fill the test hook dropped
             const uint64_t pol_kv = l2_policy_evict_last();   // K, V of a head serve all its query tiles
             const uint64_t pol_q = l2_policy_evict_first();
             for (int k = 0;; ++k) {
@@ -919,6 +882,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(item_full(slot));
                 if (w >= p.n_items) break;
                 if (!wait_bar(qdo_empty, (qf & 1) ^ 1, ctl)) break;
+                // the item's query tile starts inside its sequence and its heads exist
+                if (!FA_CHECK(it.qt >= 0 && it.qt * 128 < it.T && it.bh >= 0 && it.bh < p.BH && it.bh_kv >= 0 &&
+                                  it.bh_kv < p.BH / p.group,
+                              &g_status_bwd, abort_flag))
+                    break;
                 mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
                 ++qf;
                 int qy, qz;
@@ -931,20 +899,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int j = 0; j < it.n; ++j) {
                     {
                         const int st = kf % NKS;
-                        if (!wait_bar(k_empty(st), ((kf / NKS) & 1) ^ 1, ctl)) {
+                        if (!wait_bar(k_empty(st), ((kf / NKS) & 1) ^ 1, ctl) ||
+                            !FA_CHECK(j * kBN < it.T && st < NKS && C::kKOff + (st + 1) * C::kTileBytes <= C::kVOff,
+                                      &g_status_bwd, abort_flag)) {
                             fail = true;
                             break;
                         }
-                        mbar_arrive_expect_tx(k_full(st), C::kTileBytes);
-                        ++kf;
-                        int ky, kz;
-                        tile_yz(it, j * kBN, it.bh_kv, ky, kz);
-                        for (int a = 0; a < C::kAtomsD; ++a)
-                            tma_load_3d_hint(sK(st) + a * 128 * 128, &tm_k, k_full(st), 64 * a, ky, kz, pol_kv);
+                        if (kf == 0 && p.inject == 3 && blockIdx.x == 0) {  // test hook: never deliver this tile
+                            k_skipped = static_cast<int>(kf++);
+                        } else {
+                            mbar_arrive_expect_tx(k_full(st), C::kTileBytes);
+                            ++kf;
+                            int ky, kz;
+                            tile_yz(it, j * kBN, it.bh_kv, ky, kz);
+                            for (int a = 0; a < C::kAtomsD; ++a)
+                                tma_load_3d_hint(sK(st) + a * 128 * 128, &tm_k, k_full(st), 64 * a, ky, kz, pol_kv);
+                        }
                     }
                     {
                         const int st = vf % NVS;
-                        if (!wait_bar(v_empty(st), ((vf / NVS) & 1) ^ 1, ctl)) {
+                        if (!wait_bar(v_empty(st), ((vf / NVS) & 1) ^ 1, ctl) ||
+                            !FA_CHECK(st < NVS && C::kVOff + (st + 1) * C::kTileBytes <= C::kBarOff, &g_status_bwd,
+                                      abort_flag)) {
                             fail = true;
                             break;
                         }
@@ -962,7 +938,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             volatile int never = 0;
             Ctl drain{&never, 100000000ull};
             if (qf) wait_bar(qdo_full, (qf - 1) & 1, drain);
-            for (uint32_t f = kf > NKS ? kf - NKS : 0; f < kf; ++f) wait_bar(k_full(f % NKS), (f / NKS) & 1, drain);
+            for (uint32_t f = kf > NKS ? kf - NKS : 0; f < kf; ++f)
+                if (static_cast<int>(f) != k_skipped) wait_bar(k_full(f % NKS), (f / NKS) & 1, drain);
             for (uint32_t f = vf > NVS ? vf - NVS : 0; f < vf; ++f) wait_bar(v_full(f % NVS), (f / NVS) & 1, drain);
         }
     } else if (warp == 9) {
@@ -1026,13 +1003,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!issue_dp(vc)) goto mma_teardown;
                 if (it.n > 1 && !issue_s(kc + 1, sc + 1)) goto mma_teardown;
                 for (int j = 0; j < it.n; ++j) {
-                    FA_TRACE_EVENT(12, j);
                     if (!wait_all(ds_full, dsc & 1, ctl)) goto mma_teardown;
                     ++dsc;
-                    FA_TRACE_EVENT(13, j);
                     tc_fence_after();
                     if (j + 1 < it.n && !issue_dp(vc + j + 1)) goto mma_teardown;
-                    FA_TRACE_EVENT(18, j);
                     if (j == it.n - 1 && leader) mma_commit(qdo_empty);  // every S and dP of the item is issued
                     if (j == 0) {
                         // the previous item's dQ must have left TMEM
@@ -1045,9 +1019,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (leader) mma_ts_d(tmem + C::kDQ, tmem + C::kS(b) + C::kDSCol + s * 8, dK_mn,
                                  ks * kTile16 + s * (2048 >> 4), C::kIdescDQ, (j > 0 || s > 0) ? 1u : 0u);
                     if (leader) mma_commit(k_empty(ks));
-                    FA_TRACE_EVENT(19, j);
                     if (j + 2 < it.n && !issue_s(kc + j + 2, sc + j + 2)) goto mma_teardown;
-                    FA_TRACE_EVENT(14, j);
                 }
                 if (leader) mma_commit(dq_full);
                 kc += it.n;
@@ -1056,7 +1028,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ++item_no;
             }
         mma_teardown:
-            FA_CTA_EVENT(1, 2, globaltimer_ns());
             if (leader) {
                 mma_commit(mma_done);
                 volatile int never = 0;
@@ -1086,6 +1057,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dq_item_at<CAUSAL>(w, p, w_bh, w_qt);
             const Item it = item(w_bh, w_qt);
             const int q = it.qt * 128 + r;
+            if (!FA_CHECK(it.bh >= 0 && it.bh < p.BH && q < p.T_pad, &g_status_bwd, abort_flag)) goto compute_done;
             // -LSE2 and -D of this row (0 on padded rows q >= T, which the mask zeroes anyway)
             const float nlse = p.lse2[static_cast<size_t>(it.bh) * p.T_pad + q];
             const float nd = p.dvec[static_cast<size_t>(it.bh) * p.T_pad + q];
@@ -1093,8 +1065,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int j = 0; j < it.n; ++j) {
                 const uint32_t g = sc + j, b = g & 1;
                 const bool masked = bwd_tile_class(it.T, CAUSAL, 128, it.qt, j) == kMasked;
-                if (!warp_wait<kCritSleep>(s_full(b), (g >> 1) & 1, ctl)) goto compute_done;
-                if (warp == 0 && lane == 0) FA_TRACE_EVENT(15, j);
+                if (!warp_wait<false>(s_full(b), (g >> 1) & 1, ctl)) goto compute_done;
                 tc_fence_after();
                 uint32_t sr[64];
                 tmem_ld32(lane_base + C::kS(b) + 64 * h, sr);
@@ -1121,8 +1092,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     for (int e = 0; e < 64; ++e)
                         if (!bwd_elem_visible(it.T, CAUSAL, q, key0 + e)) pf[e] = 0.f;
                 }
-                if (!warp_wait<kCritSleep>(dp_full, (vc + j) & 1, ctl)) goto compute_done;
-                if (warp == 0 && lane == 0) FA_TRACE_EVENT(16, j);
+                if (!warp_wait<false>(dp_full, (vc + j) & 1, ctl)) goto compute_done;
                 tc_fence_after();
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
@@ -1145,7 +1115,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ds_full);
-                if (warp == 0 && lane == 0) FA_TRACE_EVENT(17, j);
             }
             sc += it.n;
             vc += it.n;
@@ -1189,7 +1158,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
-        if (lane == 0) FA_CTA_EVENT(1, 3, globaltimer_ns());
     }
     // This grid may have started while the dK/dV grid was still running (the
     // two read the same inputs and write disjoint outputs).  It ends only after
@@ -1298,6 +1266,7 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     p.prescale = p.sl2 > 0.f ? 0 : 1;
     p.sl2_eff = p.prescale ? 1.f : p.sl2;
     p.timeout_ns = dbg.timeout_ns;
+    p.inject = dbg.inject;
     p.cu_seqlens = nullptr;
     p.n_seq = 1;
     p.total = 0;
@@ -1359,6 +1328,7 @@ int run_bwd_varlen(const void* q, const void* k, const void* v, const void* o, c
     p.prescale = p.sl2 > 0.f ? 0 : 1;
     p.sl2_eff = p.prescale ? 1.f : p.sl2;
     p.timeout_ns = dbg.timeout_ns;
+    p.inject = dbg.inject;
     p.cu_seqlens = cu_seqlens;
     p.n_seq = n_seq;
     p.total = total;
@@ -1430,7 +1400,9 @@ void* g_scratch_ptr[kScratchMaxDevices];
 cudaError_t g_scratch_err[kScratchMaxDevices];
 
 // Device address of g_bwd_scratch on the current device, looked up once per
-// device (the first fa_bwd_noalloc call on that device does it).
+// device (the first fa_bwd_noalloc call on that device does it) and kept for
+// the process lifetime: it belongs to the context current at that first
+// call, and is stale after cudaDeviceReset or in another context.
 void* scratch_address(int dev) {
     std::call_once(g_scratch_once[dev], [dev] {
         void* p = nullptr;
@@ -1452,17 +1424,6 @@ int launch_bwd_noalloc(const void* q, const void* k, const void* v, const void* 
     // the preprocess kernel rewrites both vectors, so the previous call's contents do not matter
     return run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, T, D, scale, causal, ws, stream, dbg, num_sms);
 }
-
-#ifdef FA_TRACE
-// Copies the trace of the last traced launch (kTraceSlots x kTraceLen cycle stamps).
-extern "C" int fa_trace_read(unsigned long long* host) {
-    return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -5;
-}
-// Copies the per-CTA timelines (2 x kCtaTraceMax x 4 values).
-extern "C" int fa_cta_trace_read(unsigned long long* host) {
-    return cudaMemcpyFromSymbol(host, g_cta_trace, sizeof(g_cta_trace)) == cudaSuccess ? 0 : -5;
-}
-#endif
 
 int bwd_take_status() {
     int h = 0, z = 0;

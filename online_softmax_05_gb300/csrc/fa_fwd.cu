@@ -28,6 +28,7 @@
 // running max the dominant weight is exp2(0) = 1, exact in bf16.
 #include <cuda_runtime.h>
 
+#include "fa_check.cuh"
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 #include "fa_sched.h"
@@ -37,29 +38,7 @@ namespace fa {
 
 static __device__ int g_status_fwd;
 
-// Optional cycle tracing of one CTA's first work item (build with
-// -DFA_TRACE; off in the library): slot = event kind, index = key tile.
-#ifdef FA_TRACE
-constexpr int kFTraceSlots = 12, kFTraceLen = 128;
-static __device__ unsigned long long g_ftrace[kFTraceSlots][kFTraceLen];
-#define FA_FTRACE(slot, idx)                                                                     \
-    do {                                                                                         \
-        if (blockIdx.x == 0 && k == 0 && (idx) < kFTraceLen) g_ftrace[slot][idx] = clock64();     \
-    } while (0)
-#else
-#define FA_FTRACE(slot, idx) \
-    do {                     \
-    } while (0)
-#endif
-
 namespace {
-
-#ifndef FA_CRIT_SLEEP
-#define FA_CRIT_SLEEP 0
-#endif
-// Waits on the MMA <-> softmax critical path poll back to back unless built
-// with FA_CRIT_SLEEP=1; every other wait lets the hardware park the thread.
-constexpr bool kCritSleep = FA_CRIT_SLEEP != 0;
 
 constexpr int kFwdThreads = 320;
 constexpr float kRescaleThreshold = 0.0f;  // log2 units; see the rescale policy above
@@ -310,9 +289,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     if (t == 1 && !valid1) continue;
                     if (!wait_bar(q_empty(t), (q_cnt[t] & 1) ^ 1, ctl)) goto producer_done;
                     ++q_cnt[t];
+                    const int qrow = item.row0 + item.tile[t] * kFwdBM;
+                    // the tile starts inside its sequence and its head exists
+                    if (!FA_CHECK(item.tile[t] * kFwdBM < item.T && qrow < (VARLEN ? p.total : p.T) &&
+                                      item.bh[t] >= 0 && item.bh[t] < p.BH,
+                                  &g_status_fwd, abort_flag))
+                        goto producer_done;
                     mbar_arrive_expect_tx(q_full(t), C::kTileBytes);
                     ++q_armed[t];
-                    const int qrow = item.row0 + item.tile[t] * kFwdBM;
                     for (int a = 0; a < C::kAtoms; ++a)
                         tma_load_3d_hint(sQ[t] + a * C::kAtomBytes, &tm_q, q_full(t), 64 * a,
                                          VARLEN ? item.bh[t] : qrow, VARLEN ? qrow : item.bh[t], pol_q);
@@ -327,9 +311,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             skipped_fill = static_cast<int>(kv_cnt - 1);
                             continue;
                         }
+                        const int krow = item.row0 + j * kBN;
+                        // the key tile is one this query tile needs, inside the tensor, and its ring
+                        // stage lies inside the shared-memory window
+                        if (!FA_CHECK(j * kBN < item.T && bh >= 0 && bh < p.BH / p.group &&
+                                          C::kKVOff + (slot + 1) * C::kTileBytes <= C::kBarOff,
+                                      &g_status_fwd, abort_flag)) {
+                            --kv_cnt;  // nothing was armed: the drain must not wait for this fill
+                            goto producer_done;
+                        }
                         mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
                         const CUtensorMap* tm = kind ? &tm_v : &tm_k;
-                        const int krow = item.row0 + j * kBN;
                         for (int a = 0; a < C::kAtoms; ++a)
                             tma_load_3d_hint(sKV + slot * C::kTileBytes + a * C::kAtomBytes, tm, kv_full(slot),
                                              64 * a, VARLEN ? bh : krow, VARLEN ? krow : bh, pol_kv);
@@ -360,6 +352,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const SDesc dKV_mn = sdesc_make(sKV, C::kAtomBytes, 1024);
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
             auto issue_s = [&](int t, uint32_t slot) {
+                if (!FA_CHECK(t >= 0 && t < 2 && slot < C::kStages && C::kS(t) + 128 <= 512u, &g_status_fwd, abort_flag))
+                    return;
                 const uint32_t qo = t * kTile16, ko = slot * kTile16;
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
@@ -369,6 +363,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             };
             // half h of O += P V: keys 64h .. 64h+63 (k-steps 4h .. 4h+3)
             auto issue_pv_half = [&](int t, uint32_t slot, bool acc, int h) {
+                if (!FA_CHECK(t >= 0 && t < 2 && slot < C::kStages && C::kO(t) + D <= 512u, &g_status_fwd, abort_flag))
+                    return;
                 const uint32_t vo = slot * kTile16;
 #pragma unroll
                 for (int s = 4 * h; s < 4 * h + 4; ++s)
@@ -419,7 +415,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         tc_fence_after();
                         issue_pv_half(t, vs, j > 0, 0);
                         if (!wait_all(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
-                        FA_FTRACE(0 + t, j);
                         ++p_cnt[t];
                         tc_fence_after();
                         issue_pv_half(t, vs, true, 1);
@@ -434,7 +429,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         } else {
                             if (leader) mma_commit(o_full(t));
                         }
-                        FA_FTRACE(2 + t, j);
                     }
                     if (leader) mma_commit(kv_empty(vs));
                     if (has_next) {
@@ -465,6 +459,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t tS = lane_base + C::kS(t), tO = lane_base + C::kO(t);
         uint32_t s_cnt = 0, o_cnt = 0, epi_cnt = 0;
         const float eff = p.sl2_eff;
+        if (!FA_CHECK(t < 2 && C::kS(t) + 128 <= 512u && C::kO(t) + D <= 512u, &g_status_fwd, abort_flag))
+            goto softmax_done;
         for (int k = 0;; ++k) {
             int w = item_of(k, p.n_items);
             if (w < 0) break;
@@ -475,8 +471,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int n = fwd_num_kv_tiles(T, CAUSAL, tile);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
-                if (!warp_wait<kCritSleep>(s_full(t), s_cnt & 1, ctl)) goto softmax_done;
-                if (wq == 0 && lane == 0) FA_FTRACE(4 + t, j);
+                if (!warp_wait<false>(s_full(t), s_cnt & 1, ctl)) goto softmax_done;
                 ++s_cnt;
                 tc_fence_after();
                 uint32_t sr[128];
@@ -511,7 +506,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                        fmaxf(mx8[6], mx8[7]));
                 const float m_tile = mx * eff;
-                if (wq == 0 && lane == 0) FA_FTRACE(6 + t, j);
                 const float m_new = fmaxf(m_used, m_tile);
                 float alpha = 1.f;
                 bool need = false;
@@ -584,8 +578,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(t));
-                if (wq == 0 && lane == 0) FA_FTRACE(8 + t, j);
-                if (wq == 3 && lane == 0) FA_FTRACE(10 + t, j);
             }
             // ---- epilogue: O = acc / l through shared memory and a TMA store; LSE per row
             if (!warp_wait(o_full(t), o_cnt & 1, ctl)) goto softmax_done;
@@ -649,7 +641,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(epi_bar(t));
                 if (wq == 0 && lane == 0) {
-                    if (wait_bar(epi_bar(t), epi_cnt & 1, ctl)) {
+                    if (wait_bar(epi_bar(t), epi_cnt & 1, ctl) &&
+                        FA_CHECK(tile * kFwdBM < T && bh >= 0 && bh < p.BH, &g_status_fwd, abort_flag)) {
                         for (int a = 0; a < C::kAtoms; ++a)
                             tma_store_3d(&tm_o, sQ[t] + a * C::kAtomBytes, 64 * a, tile * kFwdBM, bh);
                         bulk_commit();
@@ -658,7 +651,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     mbar_arrive(q_empty(t));
                 }
                 ++epi_cnt;
-                if (row < T) p.lse[static_cast<size_t>(bh) * T + row] = (m_used + __log2f(l)) * kLn2;
+                if (row < T && FA_CHECK(bh < p.BH, &g_status_fwd, abort_flag))
+                    p.lse[static_cast<size_t>(bh) * T + row] = (m_used + __log2f(l)) * kLn2;
             }
         }
     softmax_done:;
@@ -769,12 +763,6 @@ int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, floa
     return causal ? launch_fwd_t<128, true, true>(tq, tk, tv, tq, p, grid, stream)
                   : launch_fwd_t<128, false, true>(tq, tk, tv, tq, p, grid, stream);
 }
-
-#ifdef FA_TRACE
-extern "C" int fa_ftrace_read(unsigned long long* host) {
-    return cudaMemcpyFromSymbol(host, g_ftrace, sizeof(g_ftrace)) == cudaSuccess ? 0 : -5;
-}
-#endif
 
 int fwd_take_status() {
     int h = 0, z = 0;

@@ -15,6 +15,7 @@ struct DebugKnobs {
 constexpr int kStatusTimeout = -7;
 constexpr int kStatusBadSeqlen = -11;
 constexpr int kStatusSmemAlign = -4;  // a kernel's dynamic shared-memory window was not 1024-byte aligned
+constexpr int kStatusDebugCheck = -12;  // debug build: a run-time index failed its bounds check
 
 // Launchers: arguments already validated by the C-ABI layer.
 // Hq query heads share Hkv key/value heads (Hq % Hkv == 0; Hkv == Hq is plain attention).

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_strerror_covers_codes(lib):
-    for code in range(0, -12, -1):
+    for code in range(0, -13, -1):
         s = fa.fa_strerror(code)
         assert s and "unknown" not in s
     assert "unknown" in fa.fa_strerror(-1234)

@@ -1,8 +1,14 @@
 """Failure detection without a GPU fault: every in-kernel wait is bounded.
-The forward's load warp is told (host-side test hook) to skip one tile copy;
-the kernel's waits run out after a short limit, it records
-FA_ERR_DEVICE_TIMEOUT and exits cleanly, and the context stays usable (the
-next call succeeds and is correct)."""
+
+A host-side test hook tells one kernel's load warp to skip one tile copy:
+  mode 1  the forward's load warp, its first K/V copy;
+  mode 2  the first dK/dV CTA of the backward, its first Q copy;
+  mode 3  the first dQ CTA of the backward, its first K copy.
+The waits that need the missing tile run out after a short limit, the CTA
+records FA_ERR_DEVICE_TIMEOUT, drains its copies and MMAs in flight, frees
+its tensor memory and exits.  The context stays usable: the status word is
+cleared by the read, and the next call (on every SM, so also on the SM whose
+CTA gave up) runs and matches the oracle."""
 import math
 
 import numpy as np
@@ -12,14 +18,30 @@ import torch
 import oracle
 import online_softmax_05_gb300 as fa
 from online_softmax_05_gb300.inputs import make_inputs, to_f64
-from tests.tolerances import o_ok
+from tests.tolerances import grad_bound, o_ok
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from online_softmax_05_gb300 import build
+    build.build()
+    return fa.load_library()
+
+
+def _inject(lib, mode, fn):
+    """Run fn() with the hook set and a 100 ms wait limit; restore both."""
+    assert lib.fa_debug_set_wait_timeout_ns(100_000_000) == 0
+    assert lib.fa_debug_inject(mode) == 0
+    try:
+        fn()
+        torch.cuda.synchronize()
+    finally:
+        lib.fa_debug_inject(0)
+        lib.fa_debug_set_wait_timeout_ns(2_000_000_000)
 
 
 @pytest.mark.gpu
-def test_skipped_copy_reports_timeout_and_recovers():
-    from online_softmax_05_gb300 import build
-    build.build()
-    lib = fa.load_library()
+def test_skipped_copy_reports_timeout_and_recovers(lib):
     B, H, T, D = 1, 2, 300, 64
     q, k, v, _ = make_inputs(B, H, T, D, seed=1)
     dev = torch.device("cuda")
@@ -27,15 +49,12 @@ def test_skipped_copy_reports_timeout_and_recovers():
     o = torch.empty_like(qd)
     lse = torch.empty(B, H, T, device=dev)
     assert fa.fa_get_device_status() == 0
-    assert lib.fa_debug_set_wait_timeout_ns(100_000_000) == 0
-    assert lib.fa_debug_inject(1) == 0
-    try:
-        rc = fa.fa_fwd(qd, kd, vd, o, lse, B, H, T, D, 1 / math.sqrt(D), 0, torch.cuda.current_stream())
-        assert rc == 0
-        assert fa.fa_get_device_status() == -7
-    finally:
-        lib.fa_debug_inject(0)
-        lib.fa_debug_set_wait_timeout_ns(2_000_000_000)
+
+    def call():
+        assert fa.fa_fwd(qd, kd, vd, o, lse, B, H, T, D, 1 / math.sqrt(D), 0, torch.cuda.current_stream()) == 0
+
+    _inject(lib, 1, call)
+    assert fa.fa_get_device_status() == -7
     assert fa.fa_get_device_status() == 0   # the status word was cleared
     o2, lse2 = fa.attention_forward(qd, kd, vd, causal=False)
     torch.cuda.synchronize()
@@ -43,3 +62,45 @@ def test_skipped_copy_reports_timeout_and_recovers():
     o_ref, lse_ref = oracle.attn_fwd(to_f64(q), to_f64(k), to_f64(v), 1 / math.sqrt(D), False)
     assert o_ok(to_f64(o2.cpu()), o_ref)
     assert np.abs(lse2.cpu().double().numpy() - lse_ref).max() <= 1e-3
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode", [2, 3], ids=["dkdv_q_copy", "dq_k_copy"])
+@pytest.mark.parametrize("D,causal", [(64, True), (128, False)])
+def test_backward_skipped_copy_reports_timeout_and_recovers(lib, mode, D, causal):
+    B, H, T = 1, 2, 300
+    scale = 1 / math.sqrt(D)
+    q, k, v, do = make_inputs(B, H, T, D, seed=3)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    grads = [torch.empty_like(qd) for _ in range(3)]
+
+    def call():
+        rc = fa.fa_bwd(qd, kd, vd, o, dod, lse, *grads, B, H, T, D, scale, int(causal), torch.cuda.current_stream())
+        assert rc == 0
+
+    _inject(lib, mode, call)
+    assert fa.fa_get_device_status() == -7
+    assert fa.fa_get_device_status() == 0
+    # The next backward is correct, and so is one whose grids cover every SM
+    # (512 dK/dV CTAs, a persistent dQ grid), so the SM whose CTA gave up
+    # allocates tensor memory again.
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    rq, rk, rv, _ = oracle.attn_bwd(to_f64(q), to_f64(k), to_f64(v), to_f64(do), scale, causal)
+    for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert np.abs(to_f64(g.cpu()) - r).max() <= grad_bound(r), name
+    q, k, v, do = make_inputs(4, 16, 1024, D, seed=5)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    for b, h in ((0, 0), (3, 15)):
+        rq, rk, rv, _ = oracle.attn_bwd(*(to_f64(t[b, h]) for t in (q, k, v, do)), scale, causal)
+        for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            assert np.abs(to_f64(g[b, h].cpu()) - r).max() <= grad_bound(r), (name, b, h)
