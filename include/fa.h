@@ -86,9 +86,22 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   dq, dk, dv     out: (B, H, T, D) bf16 gradients of sum(dO o O) with
  *                       respect to q, k, v (overwritten, not accumulated)
  *   B, H, T, D, scale, causal: as in fa_fwd.
- * dq is accumulated in float32 across key tiles (in one kernel that walks the
- * key tiles of each query tile) and rounded to bf16 once; no global-memory
- * reductions are involved, so the result is deterministic.
+ * dq is accumulated in float32 across key tiles and rounded to bf16 once:
+ *   D = 128: in a second kernel that walks the key tiles of each query tile;
+ *     no global-memory reductions, so the result is deterministic.
+ *   D = 64, when the dk/dv grid (one CTA per 128-key tile and key/value
+ *     head) has at least one CTA per SM: by the same kernel that computes
+ *     dk and dv (key tiles outer, as "Lab 06", section 4 orders the loops),
+ *     which adds each key tile's contribution into a float32 accumulator in
+ *     the workspace with reduce-adds; the order of those additions varies
+ *     from run to run, so dq may differ in its last bits between runs (dk
+ *     and dv do not).  Smaller grids use the two-kernel form.
+ *     fa_set_deterministic(1) selects the two-kernel form at D = 64 always.
+ * Workspace: stream-ordered with cudaMallocAsync on `stream`, released before
+ * returning: two vectors of B*H*T_pad floats plus 256 bytes (T_pad = T
+ * rounded up to 128), and when dq is summed by reduce-adds (above) the
+ * float32 dq accumulator, B*H*T_pad*D floats.  FA_ERR_NOMEM if it cannot be
+ * had.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, void* dq, void* dk, void* dv,
@@ -248,8 +261,8 @@ int fa_sched_tile_rows(int D, int* bm_fwd, int* bn, int* bm_bwd);
  * fa_debug_set_wait_timeout_ns: bound of every in-kernel wait (default 2 s).
  * fa_debug_inject: 0 = off; 1 = the forward's load warp skips its first
  *   K/V tile copy; 2 = the load warp of the backward's first dK/dV CTA skips
- *   its first Q tile copy; 3 = the load warp of the backward's first dQ CTA
- *   skips its first K tile copy.  The waits that depend on the missing copy
+ *   its third Q tile copy (its first when it has fewer); 3 = the load warp of
+ *   the backward's first dQ CTA skips its first K tile copy.  The waits that depend on the missing copy
  *   run out, the CTA gives up (it waits, bounded, for its copies and MMAs in
  *   flight, frees its tensor memory and exits) and FA_ERR_DEVICE_TIMEOUT is
  *   reported instead of a hang; the outputs of that call are not valid.
@@ -258,6 +271,17 @@ int fa_sched_tile_rows(int D, int* bm_fwd, int* bn, int* bm_bwd);
  */
 int fa_debug_set_wait_timeout_ns(unsigned long long ns);
 int fa_debug_inject(int mode);
+
+/*
+ * Backward determinism (host state, read by each fa_bwd / fa_bwd_gqa call;
+ * default 0).  1: the backward never sums into global memory, so dq, dk and
+ * dv are bitwise reproducible at every D (the two-kernel form; slower at
+ * D = 64).  0: at D = 64 the backward computes dq in its dk/dv kernel and
+ * sums the key tiles' contributions with float32 reduce-adds (see fa_bwd).
+ * Returns FA_ERR_ARG unless on is 0 or 1.  fa_bwd_varlen and fa_bwd_noalloc
+ * are always deterministic.
+ */
+int fa_set_deterministic(int on);
 
 /*
  * 1 in the debug build of the library (compiled with FA_DEBUG), 0 in the

@@ -18,6 +18,7 @@ namespace {
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject{0};
+std::atomic<int> g_deterministic{0};
 std::atomic<void*> g_events[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
 
 constexpr int kMaxDevices = 64;
@@ -66,7 +67,7 @@ int current_device(int* dev_out, int* sms_out) {
 }
 
 fa::DebugKnobs knobs() {
-    fa::DebugKnobs k{g_timeout_ns.load(), g_inject.load(), {}};
+    fa::DebugKnobs k{g_timeout_ns.load(), g_inject.load(), {}, g_deterministic.load()};
     for (int i = 0; i < 5; ++i) k.ev[i] = static_cast<cudaEvent_t>(g_events[i].load());
     return k;
 }
@@ -332,6 +333,12 @@ int fa_set_timing_events(void* fwd_begin, void* fwd_end, void* bwd_begin, void* 
     g_events[2].store(bwd_begin);
     g_events[3].store(bwd_mid);
     g_events[4].store(bwd_end);
+    return FA_OK;
+}
+
+int fa_set_deterministic(int on) {
+    if (on != 0 && on != 1) return FA_ERR_ARG;
+    g_deterministic.store(on);
     return FA_OK;
 }
 

@@ -60,42 +60,64 @@ __device__ __forceinline__ uint8_t* smem_window(uint8_t* raw) {
 }
 
 // ---------------------------------------------------------------- dK / dV kernel layout
-template <int D>
+// FUSE (D = 64 only): the same kernel also computes each query tile's dQ
+// contribution dS K (dS staged in shared memory) and adds it into an fp32
+// dQ accumulator in global memory with TMA reduce-adds, so the backward needs
+// no second pass over the key tiles.
+template <int D, bool FUSE = false>
 struct DkvCfg {
+    static_assert(!FUSE || D == 64, "the fused dQ path fits in tensor memory at D = 64 only");
     static constexpr int BM = bwd_bm(D);             // query rows per inner iteration
     static constexpr int kAtomsD = D / 64;
     static constexpr int kKVBytes = 128 * D * 2;     // one K or V tile
     static constexpr int kQBytes = BM * D * 2;       // one Q or dO tile
     // Q (with its -LSE2 and -D vectors) and dO travel in separate rings.
-    static constexpr int kQStages = (D == 128) ? 2 : 4, kDOStages = (D == 128) ? 2 : 3;
+    // (FUSE: one stage less in each ring, to make room for two dS buffers)
+    static constexpr int kQStages = FUSE ? 3 : ((D == 128) ? 2 : 4);
+    static constexpr int kDOStages = FUSE ? 2 : ((D == 128) ? 2 : 3);
     static constexpr int kQStageBytes = kQBytes + 1024;  // + -LSE2[BM], -D[BM] (<= 1 KB)
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKVBytes;
     static constexpr int kQRingOff = 2 * kKVBytes;
     static constexpr int kDORingOff = kQRingOff + kQStages * kQStageBytes;
-    static constexpr int kBarOff = kDORingOff + kDOStages * kQBytes;
+    // FUSE: dS of two query tiles (bf16, 128 keys x BM queries each, queries
+    // contiguous: the MN-major A operand of dQ = dS K), then the fp32 staging of
+    // one dQ tile (BM rows x D: per compute warp 32 rows x 32 columns, 4 KB in the
+    // 128-byte swizzled layout)
+    static constexpr int kDSOff = kDORingOff + kDOStages * kQBytes;
+    static constexpr int kDSBufBytes = 128 * BM * 2;
+    static constexpr int kDSBytes = FUSE ? 2 * kDSBufBytes : 0;
+    static constexpr int kStgOff = kDSOff + kDSBytes;
+    static constexpr int kStgBytes = FUSE ? BM * D * 4 : 0;
+    static constexpr int kBarOff = kStgOff + kStgBytes;
     // kv_full, q_full[], q_empty[], do_full[], do_empty[], s_full, dp_full, p_full, ds_full, dkv_full, mma_done,
-    // epi[2]
-    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 8;
+    // epi[2]; FUSE: dq_full[2], dq_empty[2]
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 8 + (FUSE ? 4 : 0);
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kPayload = kMiscOff + 16;   // + TMEM address slot, abort flag
     static constexpr int kSlack = (kPayload + 1024 <= kSmemLimit) ? 1024 : 0;
     static constexpr int kSmemBytes = kPayload + kSlack;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+    static_assert(kDSOff % 1024 == 0 && kStgOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
     // TMEM columns: S^T, with P^T (bf16 pairs) written over the S^T columns its
     // warpgroup has already read; dP^T, with dS^T written over it the same way;
-    // dV; dK.  Both MMA operands that come from the compute warps (P^T for dV,
-    // dS^T for dK) are read from TMEM, which keeps them off shared memory: the
-    // K-major products already use its full bandwidth.
+    // dV; dK; FUSE: two dQ buffers (a query tile's dS K, 128 query lanes x D),
+    // so one is read out while the next is computed.  Both MMA operands that
+    // come from the compute warps for dV and dK (P^T, dS^T) are read from
+    // TMEM, which keeps them off shared memory: the K-major products already
+    // use its full bandwidth.
     static constexpr uint32_t kS = 0;                // S^T [128 keys][BM] fp32
     static constexpr uint32_t kP = BM / 4;           // P^T: warpgroup h at kP + 32 h
     static constexpr uint32_t kDP = BM;              // dP^T [128 keys][BM] fp32
     static constexpr uint32_t kDS = kDP + BM / 4;    // dS^T: warpgroup h at kDS + 32 h
     static constexpr uint32_t kDV = 2 * BM;          // dV [128 keys][D] fp32
     static constexpr uint32_t kDK = kDV + D;         // dK [128 keys][D] fp32
-    static_assert(kDK + D <= 512, "TMEM budget");
+    __host__ __device__ static constexpr uint32_t kDQ(int b) { return kDK + D + D * b; }
+    static_assert((FUSE ? kDK + 3 * D : kDK + D) <= 512, "TMEM budget");
     static constexpr uint32_t kIdescS = idesc_bf16_f32(128, BM, false, false);
     static constexpr uint32_t kIdescDKV = idesc_bf16_f32(128, D, false, true);
+    // dQ = dS K: M = BM queries, N = D, K = 128 keys; dS and K both MN-major
+    static constexpr uint32_t kIdescDQ = idesc_bf16_f32(BM, D, true, true);
 };
 
 // ---------------------------------------------------------------- dQ kernel layout
@@ -144,8 +166,9 @@ struct BwdParams {
     float sl2, sl2_eff;
     int prescale;
     unsigned long long timeout_ns;
-    int inject;           // test hook: 2 = the dK/dV grid's first CTA drops its first Q fill, 3 = the dQ
-                          // grid's first CTA drops its first K fill (its waits then run out)
+    int inject;           // test hook: 2 = the dK/dV grid's first CTA drops its third Q fill (its first
+                          // when it has fewer), 3 = the dQ grid's first CTA drops its first K fill (its
+                          // waits then run out)
     // Packed variable-length batch (VARLEN kernels): sequence s occupies rows
     // cu_seqlens[s] .. cu_seqlens[s+1]-1 of the (total, H, D) tensors; T above
     // is then the longest length the caller promises, and a "head" index bh
@@ -234,7 +257,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
                                                          const float* __restrict__ lse, float* __restrict__ dvec,
                                                          float* __restrict__ lse2, int BH, int T, int T_pad,
                                                          int* __restrict__ dq_next, const int* __restrict__ cu_seqlens,
-                                                         int n_seq, int H, int total) {
+                                                         int n_seq, int H, int total, float* __restrict__ dqacc) {
     constexpr int TPR = D / 8;            // threads per row
     constexpr int RPW = 32 / TPR;         // rows per warp
     if (blockIdx.x == 0 && threadIdx.x == 0) *dq_next = 0;  // the dQ kernel's item counter
@@ -278,17 +301,46 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
             dvec[r] = -acc;
             lse2[r] = (t < len) ? -lse[lrow] * kLog2e : 0.f;
         }
+        if (dqacc != nullptr && in) {  // the fused backward's fp32 dQ accumulator starts at 0
+            float4* z = reinterpret_cast<float4*>(dqacc + static_cast<size_t>(r) * D + sub * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
+// dQ = bf16(dQacc * scale) for the rows t < T of the fused backward's fp32
+// accumulator (B*H, T_pad, D); 8 elements per thread.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __restrict__ acc,
+                                                                __nv_bfloat16* __restrict__ dq, int BH, int T,
+                                                                int T_pad, float scale) {
+    constexpr int G = D / 8;
+    const long long n = static_cast<long long>(BH) * T * G;
+    for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n;
+         g += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = g / G;
+        const int c8 = static_cast<int>(g % G);
+        const long long bh = row / T, t = row % T;
+        const float4* src = reinterpret_cast<const float4*>(acc + (bh * T_pad + t) * D + c8 * 8);
+        const float4 a = src[0], b = src[1];
+        uint4 o;
+        o.x = pack_bf16x2(a.x * scale, a.y * scale);
+        o.y = pack_bf16x2(a.z * scale, a.w * scale);
+        o.z = pack_bf16x2(b.x * scale, b.y * scale);
+        o.w = pack_bf16x2(b.z * scale, b.w * scale);
+        reinterpret_cast<uint4*>(dq + row * D + c8 * 8)[0] = o;
     }
 }
 
 // ---------------------------------------------------------------- dK / dV kernel
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool FUSE = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                       BwdParams p) {
-    using C = DkvCfg<D>;
+                       const __grid_constant__ CUtensorMap tm_dqacc, BwdParams p) {
+    using C = DkvCfg<D, FUSE>;
     constexpr int BM = C::BM;
     constexpr int NQS = C::kQStages, NDS = C::kDOStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -319,6 +371,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t dkv_full = b0 + 32;  // every dK / dV MMA done
     const uint32_t mma_done = b0 + 40;
     auto epi_bar = [&](int hh) { return b0 + 48 + 8u * hh; };  // warpgroup hh staged its output (4 warps)
+    // FUSE: dQ buffer b holds a finished dS K (MMA) / was read out (8 compute warps)
+    auto dq_full = [&](int b) { return b0 + 64 + 8u * b; };
+    auto dq_empty = [&](int b) { return b0 + 80 + 8u * b; };
+    const uint32_t sDS = sbase + C::kDSOff, sStg = sbase + C::kStgOff;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
     const Ctl ctl{abort_flag, p.timeout_ns};
@@ -375,6 +431,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(mma_done, 1);
         mbar_init(epi_bar(0), 4);
         mbar_init(epi_bar(1), 4);
+        if constexpr (FUSE) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(dq_full(b), 1);
+                mbar_init(dq_empty(b), 8);
+            }
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -417,7 +479,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                       voff + BM <= static_cast<size_t>(p.BH) * p.group * p.T_pad,
                                   &g_status_bwd, abort_flag))
                         break;
-                    if (it == 0 && p.inject == 2 && blockIdx.x == 0) {  // test hook: never deliver this tile
+                    // test hook: never deliver the third Q tile (the first when there are fewer)
+                    if (it == (n_it > 2 ? 2 : 0) && p.inject == 2 && blockIdx.x == 0) {
                         q_skipped = static_cast<int>(q_armed++);
                     } else {
                         mbar_arrive_expect_tx(fb, C::kQBytes + 2 * BM * 4);
@@ -463,6 +526,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const SDesc dK_km = sdesc_make(sK, 16, 1024), dV_km = sdesc_make(sV, 16, 1024);
             const SDesc dQ_km = sdesc_make(sQ(0), 16, 1024), dO_km = sdesc_make(sdO(0), 16, 1024);
             const SDesc dQ_mn = sdesc_make(sQ(0), BM * 128, 1024), dO_mn = sdesc_make(sdO(0), BM * 128, 1024);
+            // FUSE: dS (queries contiguous, 64-query column blocks 128 x 128 B apart) and K
+            // (D contiguous) as the MN-major operands of dQ = dS K
+            const SDesc dDS_mn = sdesc_make(sDS, 128 * 128, 1024), dK_mn = sdesc_make(sK, 128 * 128, 1024);
             constexpr uint32_t kQStage16 = C::kQStageBytes >> 4, kDOStage16 = C::kQBytes >> 4;
             constexpr int NKV = BM / 16;  // k-steps of dV and dK
             // S^T = K Q^T: M = 128 keys, N = BM, K = D (both K-major)
@@ -525,6 +591,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tc_fence_after();
                     issue_dp(ds1);
                 }
+                if constexpr (FUSE) {
+                    // dQ(it) = dS(it) K into TMEM buffer it & 1, once the compute warps have
+                    // read out dQ(it - 2) from it.  dS(it) has been in shared-memory buffer
+                    // it & 1 since ds_full; issued after dP^T(it+1), so the compute warps
+                    // get dP^T(it+1) without waiting for it.
+                    const int b = it & 1;
+                    if (it >= 2 && !wait_all(dq_empty(b), ((it >> 1) - 1) & 1, ctl)) goto mma_teardown;
+                    tc_fence_after();
+                    const uint32_t dso = static_cast<uint32_t>(b * C::kDSBufBytes) >> 4;
+#pragma unroll
+                    for (int s = 0; s < 128 / 16; ++s)
+                        if (leader) mma_ss_d(tmem + C::kDQ(b), dDS_mn, dso + s * (2048 >> 4), dK_mn, s * (2048 >> 4),
+                                             C::kIdescDQ, s > 0 ? 1u : 0u);
+                    if (leader) mma_commit(dq_full(b));
+                }
             }
             if (leader) mma_commit(dkv_full);
         mma_teardown:
@@ -552,6 +633,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool prescale = p.prescale != 0;
         const uint64_t eff2 = f2(eff, eff);
         bool ok = true;
+        // FUSE: read dQ(j) = dS(j) K out of TMEM buffer j & 1 (this warpgroup's 32 of
+        // the D columns, one query row per thread), stage the warp's 32 rows in its
+        // own 4 KB of shared memory in the 128-byte swizzled layout of the
+        // accumulator's tensor map, and add them into the fp32 accumulator with
+        // one TMA reduce from lane 0.  Each warp reuses its staging only after its
+        // own previous reduce has read it, so the warps never wait for each other.
+        // Every wait is bounded; false when the CTA gave up.
+        const uint32_t stg_w = sStg + (h * 4 + wq) * 4096;
+        auto drain_dq = [&](int j) -> bool {
+            const int b = j & 1;
+            if (!warp_wait(dq_full(b), (j >> 1) & 1, ctl)) return false;
+            tc_fence_after();
+            uint32_t v[32];
+            tmem_ld32(lane_base + C::kDQ(b) + 32 * h, v);
+            tmem_ld_wait();
+            reg_fence32(v);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(dq_empty(b));
+                bulk_wait_read0();  // this warp's previous reduce has read its staging
+            }
+            __syncwarp();
+            const uint32_t rowa = stg_w + lane * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(rowa + ((c ^ (lane & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int qtj = q_tile_of(j), bhqj = q_head_of(j);
+                if (FA_CHECK(qtj * BM < T && bhqj >= 0 && bhqj < p.BH * p.group, &g_status_bwd, abort_flag)) {
+                    tma_reduce_add_3d(&tm_dqacc, stg_w, 32 * h, qtj * BM + 32 * wq, bhqj);
+                    bulk_commit();
+                }
+            }
+            return true;
+        };
         for (int it = 0; it < n_it; ++it) {
             const int st = it % NQS;
             const int qt = q_tile_of(it), q0 = qt * BM;
@@ -648,10 +767,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tmem_st_16x128b_x8(lane_base + C::kDS + 32 * h, dsw);
             tmem_st_16x128b_x8(lane_base + (16u << 16) + C::kDS + 32 * h, dsw + 16);
+            if constexpr (FUSE) {
+                // dS into shared-memory buffer it & 1 for dQ = dS K, queries contiguous:
+                // key row k of this warpgroup's 64-query block at k * 128 bytes,
+                // 16-byte chunk c (queries 8c .. 8c+7) at position c ^ (k % 8).  The
+                // registers are already in the 8 x 8 fragment layout (row = key,
+                // column pair = two queries), so each stmatrix writes four such
+                // blocks.  dQ(it - 2), the last reader of this buffer, was issued
+                // before dP^T(it), so it completed before dP^T(it) did.
+                const int rr = lane & 7, mi = lane >> 3;
+                const uint32_t sDSb = sDS + (it & 1) * C::kDSBufBytes;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                    for (int i2 = 0; i2 < 2; ++i2) {
+                        const int key = 32 * wq + 16 * hf + 8 * i2 + rr;
+                        const uint32_t rowa = sDSb + h * (128 * 128) + key * 128;
+                        const int b = 16 * hf + i2;
+#pragma unroll
+                        for (int g = 0; g < 2; ++g)
+                            stmatrix_x4(rowa + (((4 * g + mi) ^ rr) << 4), dsw[b + 8 * g], dsw[b + 8 * g + 2],
+                                        dsw[b + 8 * g + 4], dsw[b + 8 * g + 6]);
+                    }
+                fence_proxy_async_smem();
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
+            // FUSE: the previous query tile's dQ (issued after dP^T(it)) is read out
+            // while the tensor pipe runs dK(it), dP^T(it+1) and dQ(it)
+            if constexpr (FUSE) {
+                if (it > 0 && !drain_dq(it - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        if constexpr (FUSE) {
+            if (ok && n_it > 0 && !drain_dq(n_it - 1)) ok = false;
         }
         // epilogue: warpgroup 0 stores dK * scale, warpgroup 1 stores dV.  Each
         // stages its 128 x D bf16 tile in shared memory in the 128-byte swizzled
@@ -718,6 +872,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bulk_wait0();
             }
         }
+        // FUSE: the dQ reduce-adds read shared memory and must land before the CTA exits
+        if (FUSE && lane == 0) bulk_wait0();
     }
 
     tc_fence_before();
@@ -1175,6 +1331,32 @@ bool set_smem_once(K kern, int bytes, bool& done) {
     return true;
 }
 
+// The fused backward (D = 64): one dK/dV grid that also adds every query
+// tile's dQ contribution into the fp32 accumulator (zeroed by the
+// preprocess kernel), then the conversion of the accumulator to bf16 dQ.
+template <bool CAUSAL>
+int launch_fused_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                   const CUtensorMap& tdk, const CUtensorMap& tdv, const CUtensorMap& tacc, BwdParams p, int BHq,
+                   int BHkv, const float* acc, cudaStream_t st, const DebugKnobs& dbg, int num_sms) {
+    constexpr int D = 64;
+    static bool attr = false;
+    auto ka = fa_bwd_dkdv_kernel<D, CAUSAL, false, true>;
+    if (!set_smem_once(ka, DkvCfg<D, true>::kSmemBytes, attr)) return -5;
+    if (dbg.ev[2]) cudaEventRecord(dbg.ev[2], st);
+    p.BH = BHkv;
+    p.kt_major = (p.n_kt * BHkv < 8 * num_sms) ? 1 : 0;
+    ka<<<p.n_kt * BHkv, kBwdThreads, DkvCfg<D, true>::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, tacc, p);
+    if (cudaGetLastError() != cudaSuccess) return -5;
+    if (dbg.ev[3]) cudaEventRecord(dbg.ev[3], st);
+    const long long groups = static_cast<long long>(BHq) * p.T * (D / 8);
+    const long long blocks = (groups + 255) / 256;
+    const int grid = static_cast<int>(blocks < 8LL * num_sms ? blocks : 8LL * num_sms);
+    fa_bwd_dq_convert_kernel<D><<<grid, 256, 0, st>>>(acc, p.dq, BHq, p.T, p.T_pad, p.scale);
+    if (cudaGetLastError() != cudaSuccess) return -5;
+    if (dbg.ev[4]) cudaEventRecord(dbg.ev[4], st);
+    return 0;
+}
+
 template <int D, bool CAUSAL, bool VARLEN>
 int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                   const CUtensorMap& tdk, const CUtensorMap& tdv, BwdParams p, int BHq, int BHkv, cudaStream_t st,
@@ -1190,7 +1372,7 @@ int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     // 0.86 -> 0.71 ms, D = 64 T = 2048 0.129 -> 0.114 ms); head major above
     // (T = 8192, 32 heads: 0.771 vs 0.792 ms key-tile major)
     p.kt_major = (p.n_kt * BHkv < 8 * num_sms) ? 1 : 0;
-    ka<<<p.n_kt * BHkv, kBwdThreads, DkvCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, p);
+    ka<<<p.n_kt * BHkv, kBwdThreads, DkvCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, tq, p);
     if (cudaGetLastError() != cudaSuccess) return -5;
     if (dbg.ev[3]) cudaEventRecord(dbg.ev[3], st);
     p.BH = BHq;
@@ -1221,29 +1403,32 @@ int launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
 // counter) already in place.
 int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
             void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, bool causal, void* ws,
-            cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
+            bool fuse, cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
     const int BH = B * Hq, BHkv = B * Hkv;
     const int T_pad = cdiv(T, 128) * 128;
     const size_t bytes_vec = (static_cast<size_t>(BH) * T_pad * 4 + 255) / 256 * 256;
     float* dvec = static_cast<float*>(ws);
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_vec);
     int* dq_next = reinterpret_cast<int*>(static_cast<char*>(ws) + 2 * bytes_vec);
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    // fused backward: the fp32 dQ accumulator follows the item counter (256-byte aligned)
+    float* dqacc = fuse ? reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * bytes_vec + 256) : nullptr;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tacc;
     if (!make_tmap_bhtd(&tq, q, BH, T, D, 128) || !make_tmap_bhtd(&tk, k, BHkv, T, D, 128) ||
         !make_tmap_bhtd(&tv, v, BHkv, T, D, 128) || !make_tmap_bhtd(&tdo, dO, BH, T, D, 128) ||
         !make_tmap_bhtd(&tdk, dk, BHkv, T, D, 128) || !make_tmap_bhtd(&tdv, dv, BHkv, T, D, 128))
         return -5;
+    if (fuse && (D != 64 || !make_tmap_f32_acc(&tacc, dqacc, BH, T_pad, D, 32))) return -5;
     const long long rows = static_cast<long long>(BH) * T_pad;
     const long long blocks = (rows * (D / 8) + 255) / 256;
     const int pre_grid = static_cast<int>(blocks < 8LL * num_sms ? blocks : 8LL * num_sms);
     if (D == 64)
         fa_bwd_pre_kernel<64, false><<<pre_grid, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2, BH, T, T_pad,
-            dq_next, nullptr, 1, Hq, 0);
+            dq_next, nullptr, 1, Hq, 0, dqacc);
     else
         fa_bwd_pre_kernel<128, false><<<pre_grid, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2, BH, T, T_pad,
-            dq_next, nullptr, 1, Hq, 0);
+            dq_next, nullptr, 1, Hq, 0, nullptr);
     if (cudaGetLastError() != cudaSuccess) return -5;
     BwdParams p;
     p.lse2 = lse2;
@@ -1270,6 +1455,10 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     p.cu_seqlens = nullptr;
     p.n_seq = 1;
     p.total = 0;
+    if (fuse)
+        return causal ? launch_fused_t<true>(tq, tk, tv, tdo, tdk, tdv, tacc, p, BH, BHkv, dqacc, stream, dbg, num_sms)
+                      : launch_fused_t<false>(tq, tk, tv, tdo, tdk, tdv, tacc, p, BH, BHkv, dqacc, stream, dbg,
+                                              num_sms);
     if (D == 64)
         return causal ? launch_main_t<64, true, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms)
                       : launch_main_t<64, false, false>(tq, tk, tv, tdo, tdk, tdv, p, BH, BHkv, stream, dbg, num_sms);
@@ -1301,11 +1490,11 @@ int run_bwd_varlen(const void* q, const void* k, const void* v, const void* o, c
     if (D == 64)
         fa_bwd_pre_kernel<64, true><<<pre_grid, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2, BH,
-            max_seqlen, T_pad, dq_next, cu_seqlens, n_seq, H, total);
+            max_seqlen, T_pad, dq_next, cu_seqlens, n_seq, H, total, nullptr);
     else
         fa_bwd_pre_kernel<128, true><<<pre_grid, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, dvec, lse2, BH,
-            max_seqlen, T_pad, dq_next, cu_seqlens, n_seq, H, total);
+            max_seqlen, T_pad, dq_next, cu_seqlens, n_seq, H, total, nullptr);
     if (cudaGetLastError() != cudaSuccess) return -5;
     BwdParams p;
     p.lse2 = lse2;
@@ -1349,6 +1538,17 @@ size_t bwd_scratch_bytes(int B, int H, int T, int D) {
     const size_t bytes_vec = (BH * T_pad * 4 + 255) / 256 * 256;
     return 2 * bytes_vec + 256;  // + the dQ kernel's item counter
 }
+// The fused backward (D = 64) when it fills the GPU: with fewer dK/dV CTAs
+// than SMs the two-kernel form is faster, its dQ grid running on the SMs the
+// dK/dV grid leaves idle (B=1 H=8 T=1024: 24 us two-kernel, 32 us fused).
+bool bwd_fuses(int D, int n_kt, int BHkv, int num_sms, const DebugKnobs& dbg) {
+    return D == 64 && !dbg.deterministic && static_cast<long long>(n_kt) * BHkv >= num_sms;
+}
+size_t bwd_workspace_bytes(int B, int H, int T, int D, bool fuse) {
+    const size_t T_pad = static_cast<size_t>(cdiv(T, 128)) * 128;
+    // fused: + the fp32 dQ accumulator (B*H, T_pad, D)
+    return bwd_scratch_bytes(B, H, T, D) + (fuse ? static_cast<size_t>(B) * H * T_pad * D * 4 : 0);
+}
 
 size_t bwd_varlen_scratch_bytes(int n_seq, int H, int max_seqlen) {
     const size_t BH = static_cast<size_t>(n_seq) * H;
@@ -1375,12 +1575,14 @@ int launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T, int D, float scale, bool causal,
                cudaStream_t stream, const DebugKnobs& dbg, int num_sms) {
+    const bool fuse = bwd_fuses(D, cdiv(T, kBN), B * Hkv, num_sms, dbg);
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, bwd_scratch_bytes(B, Hq, T, D), stream) != cudaSuccess) {
+    if (cudaMallocAsync(&ws, bwd_workspace_bytes(B, Hq, T, D, fuse), stream) != cudaSuccess) {
         cudaGetLastError();
         return -6;
     }
-    int rc = run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, T, D, scale, causal, ws, stream, dbg, num_sms);
+    int rc = run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, T, D, scale, causal, ws, fuse, stream, dbg,
+                     num_sms);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == 0) rc = -5;
     return rc;
 }
@@ -1422,7 +1624,7 @@ int launch_bwd_noalloc(const void* q, const void* k, const void* v, const void* 
     void* ws = scratch_address(dev);
     if (!ws) return -5;
     // the preprocess kernel rewrites both vectors, so the previous call's contents do not matter
-    return run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, T, D, scale, causal, ws, stream, dbg, num_sms);
+    return run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, T, D, scale, causal, ws, false, stream, dbg, num_sms);
 }
 
 int bwd_take_status() {

@@ -9,6 +9,7 @@ struct DebugKnobs {
     unsigned long long timeout_ns;  // bound of every in-kernel wait
     int inject;                     // fault-injection mode (0 = off)
     cudaEvent_t ev[5];              // measurement hook: fwd begin/end; bwd: before dK/dV, between, after dQ (may be null)
+    int deterministic;              // 1: the backward never sums into global memory (two-kernel form at every D)
 };
 
 // Status word values written by kernels (mirror of fa_status).

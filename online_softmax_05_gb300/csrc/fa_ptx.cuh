@@ -99,6 +99,23 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// 3-D tiled reduce-add from shared memory into global memory (element type
+// and layout from the tensor map; here fp32 add).  Completion is tracked by
+// the bulk async-group of the issuing thread.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+// Four 8 x 8 b16 matrices from the warp's registers to shared memory: lane j
+// gives the address of row j % 8 of matrix j / 8; register i of lane t holds
+// row t / 4, columns 2 (t % 4) and 2 (t % 4) + 1 of matrix i.
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

@@ -43,6 +43,22 @@ inline bool make_tmap_bhtd(CUtensorMap* map, const void* base, int BH, int T, in
     return r == CUDA_SUCCESS;
 }
 
+// (BH, T_pad, D) fp32 accumulator viewed as {D, T_pad, BH} with boxes of 32
+// columns (128 bytes) x box_rows rows and 128-byte swizzle: the target of the
+// fused backward's dQ reduce-adds.
+inline bool make_tmap_f32_acc(CUtensorMap* map, const void* base, int BH, int T_pad, int D, int box_rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T_pad), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(T_pad) * D * 4};
+    cuuint32_t box[3] = {32u, static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Packed variable-length layout (total, H, D) bf16: dimensions (D, H, total)
 // with strides (2 B, D*2 B, H*D*2 B), boxes of 64 columns x 1 head x
 // box_rows rows.  The box lands in shared memory exactly as a

@@ -25,3 +25,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def deterministic_backward():
+    """Run the test with the library's deterministic backward (no sums in
+    global memory at any head size), then restore the default."""
+    import online_softmax_05_gb300 as fa
+    from online_softmax_05_gb300 import build
+    build.build()
+    lib = fa.load_library()
+    assert lib.fa_set_deterministic(1) == 0
+    try:
+        yield
+    finally:
+        lib.fa_set_deterministic(0)
+

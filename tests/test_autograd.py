@@ -10,7 +10,7 @@ import oracle
 import online_softmax_05_gb300 as fa
 from online_softmax_05_gb300.inputs import make_inputs, to_f64
 
-from tests.tolerances import grad_bound, o_ok
+from tests.tolerances import grad_bound, o_ok, same_gradients, same_up_to_sum_order
 
 
 def test_cpu_tensors_are_refused():
@@ -43,8 +43,7 @@ def test_gradients_match_oracle_and_direct_calls(D, causal):
     o2, lse2 = fa.attention_forward(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
     g2 = fa.attention_backward(q.cuda(), k.cuda(), v.cuda(), o2, lse2, do.cuda(), causal=causal, scale=scale)
     assert torch.equal(o.detach(), o2)
-    for got, want in zip((ql.grad, kl.grad, vl.grad), g2):
-        assert torch.equal(got, want)
+    assert same_gradients((ql.grad, kl.grad, vl.grad), g2, D)
     # and within tolerance of the oracle
     qf, kf, vf, df = (to_f64(t) for t in (q, k, v, do))
     o_ref, _ = oracle.attn_fwd(qf, kf, vf, scale, causal)
@@ -68,5 +67,6 @@ def test_three_dimensional_form_is_one_head():
     torch.cuda.synchronize()
     assert o3.shape == (2, 300, 64)
     assert torch.equal(o3.detach(), o4.detach()[:, 0])
-    for a, b in ((q3, q4), (k3, k4), (v3, v4)):
+    assert same_up_to_sum_order(q3.grad, q4.grad[:, 0])   # D = 64: dQ sums in varying order
+    for a, b in ((k3, k4), (v3, v4)):
         assert torch.equal(a.grad, b.grad[:, 0])

@@ -109,7 +109,7 @@ def test_backward_head_pair_schedule_odd_tile_count():
 @pytest.mark.gpu
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_work_partition_does_not_change_bits_backward(D, causal):
+def test_work_partition_does_not_change_bits_backward(D, causal, deterministic_backward):
     # 4 heads of T = 2048 make few dK/dV CTAs, launched key tile major; 32 x 4
     # heads make many, launched head by head; the dQ kernel hands its items out
     # in whatever order CTAs ask.  Each key tile's dK / dV and each query tile's
@@ -155,3 +155,38 @@ def test_long_sequence_sampled_rows(D, causal):
     check("dq", to_f64(dq[0, 0].cpu())[rows], rq)
     check("dk", to_f64(dk[0, 0].cpu())[rows], rk)
     check("dv", to_f64(dv[0, 0].cpu())[rows], rv)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_fused_backward_against_the_two_kernel_form(causal):
+    # D = 64 by default computes dQ inside the dK/dV kernel and sums the key
+    # tiles' contributions with float32 reduce-adds.  dK and dV come from the
+    # same per-key-tile arithmetic as the two-kernel form and must match it bit
+    # for bit.  dQ is built from the dK/dV kernel's own dS (rounded to bf16
+    # there, not in a second kernel), so the two forms' dQ are each checked
+    # against the oracle; two fused runs differ only in the order of the same
+    # float32 sums.  The batch's grid covers every SM (64 heads).
+    from tests.tolerances import same_up_to_sum_order
+    B, H, T, D = 4, 16, 1000, 64
+    q, k, v, do = make_inputs(B, H, T, D, seed=27)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal)
+    fused = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal)
+    fused2 = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal)
+    lib = fa.load_library()
+    assert lib.fa_set_deterministic(1) == 0
+    try:
+        two = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal)
+    finally:
+        lib.fa_set_deterministic(0)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    assert torch.equal(fused[1], two[1]) and torch.equal(fused[2], two[2])
+    assert same_up_to_sum_order(fused[0], fused2[0])
+    for b, h in ((0, 0), (1, 7), (3, 15)):
+        rq, rk, rv, _ = oracle.attn_bwd(*(to_f64(t[b, h]) for t in (q, k, v, do)), D ** -0.5, causal)
+        check("dq fused", to_f64(fused[0][b, h].cpu()), rq)
+        check("dq two-kernel", to_f64(two[0][b, h].cpu()), rq)
+

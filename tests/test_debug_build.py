@@ -8,7 +8,8 @@ Host side: the debug library exports every symbol include/fa.h declares and
 says it is the debug build.  GPU side: the small parity cases (both masks,
 both head dimensions, ragged tails, grouped heads, a packed batch) run
 through the debug library with no check failing, and its results equal the
-product library's bit for bit (the checks change no arithmetic)."""
+product library's bit for bit (the checks change no arithmetic; dQ of the
+D = 64 backward up to the order of its float32 sums)."""
 import ctypes
 import math
 import os
@@ -21,7 +22,7 @@ import oracle
 import online_softmax_05_gb300 as fa
 from online_softmax_05_gb300.inputs import make_inputs, to_f64
 from tests.test_abi import declared_functions
-from tests.tolerances import LSE_TOL, grad_bound, o_ok
+from tests.tolerances import LSE_TOL, grad_bound, o_ok, same_gradients
 
 PKG = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "online_softmax_05_gb300")
 
@@ -79,8 +80,7 @@ def test_debug_build_runs_small_cases_clean(dlib, T, causal, D):
     g2 = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
     torch.cuda.synchronize()
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
-    for a, b in zip((dq, dk, dv), g2):
-        assert torch.equal(a, b)
+    assert same_gradients((dq, dk, dv), g2, D)
     # and the oracle agrees
     o_ref, lse_ref = oracle.attn_fwd(to_f64(q), to_f64(k), to_f64(v), scale, causal)
     assert o_ok(to_f64(o.cpu()), o_ref)

