@@ -92,3 +92,21 @@ def test_gqa_longer_sequence():
     rq, rk, rv, _ = oracle.attn_bwd_gqa(qf, kf, vf, df, scale, True)
     for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         assert np.abs(g - r).max() <= grad_bound(r), name
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_fused_backward_full_grid(causal):
+    # D = 64 with at least one dK/dV CTA per SM (4 batches x 4 K/V heads x 10
+    # key tiles = 160): the backward sums dQ with reduce-adds inside the dK/dV
+    # kernel, walking the query tiles of all 4 query heads of each group.
+    # Batches are independent, so the oracle checks the first and the last.
+    B, Hq, Hkv, T, D = 4, 16, 4, 1280, 64
+    q, k, v, do = make(B, Hq, Hkv, T, D, seed=12)
+    scale = D ** -0.5
+    o, dq, dk, dv, lse = run(q, k, v, do, causal, scale)
+    for b in (0, B - 1):
+        qf, kf, vf, df = (to_f64(t[b:b + 1]) for t in (q, k, v, do))
+        rq, rk, rv, _ = oracle.attn_bwd_gqa(qf, kf, vf, df, scale, causal)
+        for name, g, r in (("dq", dq[b:b + 1], rq), ("dk", dk[b:b + 1], rk), ("dv", dv[b:b + 1], rv)):
+            assert np.abs(g - r).max() <= grad_bound(r), (name, b)
