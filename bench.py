@@ -49,6 +49,7 @@ KERNEL_SOURCES = {
     "fa_fwd_kernel": ["online_softmax_05_gb300/csrc/fa_fwd.cu"],
     "fa_bwd_dkdv_kernel": ["online_softmax_05_gb300/csrc/fa_bwd.cu"],
     "fa_bwd_dq_kernel": ["online_softmax_05_gb300/csrc/fa_bwd.cu"],
+    "fa_bwd_dq_convert_kernel": ["online_softmax_05_gb300/csrc/fa_bwd.cu"],
 }
 COMMON_SOURCES = ["online_softmax_05_gb300/csrc/fa_ptx.cuh", "online_softmax_05_gb300/csrc/fa_sched.h",
                   "online_softmax_05_gb300/csrc/fa_tmap.h"]
@@ -662,8 +663,12 @@ def main():
     # Algorithmic FLOPs per backward kernel: of the backward's five products
     # (S, dP, dV, dK, dQ; 2.5x the forward) the dK/dV kernel performs four
     # (2x the forward) and the dQ kernel one (0.5x); the dQ kernel's
-    # recomputation of S and dP is extra work and is not counted.
-    dkdv_tflops = 2.0 * fwd_fl / (dkdv_ms * 1e-3) / 1e12
+    # recomputation of S and dP is extra work and is not counted.  Where the
+    # library sums dQ inside the dK/dV kernel (D = 64 on a full grid) that
+    # kernel performs all five, and the second kernel only converts the float32
+    # dQ accumulator to bf16 (HBM-bound: 4 bytes read, 2 written per element).
+    in_place = lib.fa_bwd_sums_dq_in_place(B, H, T, D) == 1
+    dkdv_tflops = (2.5 if in_place else 2.0) * fwd_fl / (dkdv_ms * 1e-3) / 1e12
     dq_tflops = 0.5 * fwd_fl / (dq_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak_sus, peak_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
@@ -676,9 +681,17 @@ def main():
                 "frac": achieved / peak_burst, "peak_kind": f"bf16 dense, burst, of {peak_src}",
                 "frac_of_sustained": achieved / peak_sus, "traffic": recorded_traffic(kernel, w.name)}
 
+    if in_place:
+        conv_bytes = B * H * T * D * 6
+        conv_gbs = conv_bytes / (dq_ms * 1e-3) / 1e9
+        second = {"bound": "hbm", "kernel": "fa_bwd_dq_convert_kernel", "achieved": conv_gbs, "peak": peaks["hbm_gbs"],
+                  "unit": "GB/s", "frac": conv_gbs / peaks["hbm_gbs"], "peak_kind": f"copy bandwidth, of {peak_src}",
+                  "traffic": recorded_traffic("fa_bwd_dq_convert_kernel", w.name)}
+    else:
+        second = roofline("fa_bwd_dq_kernel", dq_tflops)
     rls = sorted([(fwd_ms, roofline("fa_fwd_kernel", fwd_tflops_kernel)),
                   (dkdv_ms, roofline("fa_bwd_dkdv_kernel", dkdv_tflops)),
-                  (dq_ms, roofline("fa_bwd_dq_kernel", dq_tflops))], key=lambda x: -x[0])
+                  (dq_ms, second)], key=lambda x: -x[0])
 
     # End to end through the public API with host buffers (pinned), copies timed.
     # Every step uploads its inputs (Q, K, V, dO) and downloads its results
@@ -771,6 +784,7 @@ def main():
                    "passes": "fwd+bwd", "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: inputs + outputs + workspace per step ~0.7 GB > 129 MB L2"},
         "fwd_tflops": fwd_tflops_kernel, "fwd_ms": fwd_ms, "bwd_dkdv_ms": dkdv_ms, "bwd_dq_ms": dq_ms,
+        "bwd_form": "dQ summed in the dK/dV kernel, then converted" if in_place else "dK/dV kernel, then dQ kernel",
         "bwd_tflops": bwd_tflops_kernels,
         "kernel_times": f"CUDA events around each kernel in a separate pass of {KS} steps after the timed region "
                         "(events between the backward's two grids serialise them; in the timed region the dQ grid "

@@ -284,6 +284,16 @@ int fa_debug_inject(int mode);
 int fa_set_deterministic(int on);
 
 /*
+ * Host query (no launch): 1 if fa_bwd / fa_bwd_gqa on this shape, on the
+ * current device and in the current determinism mode, computes dq inside its
+ * dk/dv kernel and sums it with reduce-adds (then its second kernel is the
+ * conversion of the float32 accumulator to bf16 dq), 0 if it runs the
+ * two-kernel form.  FA_ERR_SHAPE / FA_ERR_UNSUPPORTED for bad sizes,
+ * FA_ERR_ARCH or FA_ERR_CUDA without a suitable current device.
+ */
+int fa_bwd_sums_dq_in_place(int B, int Hkv, int T, int D);
+
+/*
  * 1 in the debug build of the library (compiled with FA_DEBUG), 0 in the
  * product build.  In the debug build every kernel checks the tile
  * coordinates, ring stages, per-row vector offsets and tensor-memory columns

@@ -82,6 +82,8 @@ def load_library():
         lib.fa_debug_set_wait_timeout_ns.restype = i
         lib.fa_debug_inject.argtypes = [i]
         lib.fa_debug_inject.restype = i
+        lib.fa_bwd_sums_dq_in_place.argtypes = [i, i, i, i]
+        lib.fa_bwd_sums_dq_in_place.restype = i
         lib.fa_set_deterministic.argtypes = [i]
         lib.fa_set_deterministic.restype = i
         lib.fa_set_timing_events.argtypes = [vp, vp, vp, vp, vp]

@@ -336,6 +336,15 @@ int fa_set_timing_events(void* fwd_begin, void* fwd_end, void* bwd_begin, void* 
     return FA_OK;
 }
 
+int fa_bwd_sums_dq_in_place(int B, int Hkv, int T, int D) {
+    if (B < 1 || Hkv < 1 || T < 1) return FA_ERR_SHAPE;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    const int rc = current_device(&dev, &sms);
+    if (rc != FA_OK) return rc;
+    return fa::bwd_fuses_host(B, Hkv, T, D, sms, g_deterministic.load() != 0) ? 1 : 0;
+}
+
 int fa_set_deterministic(int on) {
     if (on != 0 && on != 1) return FA_ERR_ARG;
     g_deterministic.store(on);

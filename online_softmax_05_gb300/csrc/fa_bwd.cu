@@ -1544,6 +1544,11 @@ size_t bwd_scratch_bytes(int B, int H, int T, int D) {
 bool bwd_fuses(int D, int n_kt, int BHkv, int num_sms, const DebugKnobs& dbg) {
     return D == 64 && !dbg.deterministic && static_cast<long long>(n_kt) * BHkv >= num_sms;
 }
+bool bwd_fuses_host(int B, int Hkv, int T, int D, int num_sms, bool deterministic) {
+    DebugKnobs k{};
+    k.deterministic = deterministic ? 1 : 0;
+    return bwd_fuses(D, cdiv(T, kBN), B * Hkv, num_sms, k);
+}
 size_t bwd_workspace_bytes(int B, int H, int T, int D, bool fuse) {
     const size_t T_pad = static_cast<size_t>(cdiv(T, 128)) * 128;
     // fused: + the fp32 dQ accumulator (B*H, T_pad, D)

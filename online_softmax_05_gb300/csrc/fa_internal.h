@@ -44,6 +44,8 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
 // Backward with the library's fixed device scratch buffer instead of an
 // allocation; returns -10 if the problem does not fit, without launching.
 size_t bwd_scratch_bytes(int B, int H, int T, int D);
+// Whether fa_bwd sums dQ inside the dK/dV kernel for this shape on a GPU with num_sms SMs.
+bool bwd_fuses_host(int B, int Hkv, int T, int D, int num_sms, bool deterministic);
 int launch_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                        void* dq, void* dk, void* dv, int B, int H, int T, int D, float scale, bool causal,
                        cudaStream_t stream, const DebugKnobs& dbg, int num_sms);
