@@ -131,7 +131,7 @@ def recorded_traffic(kernel, workload):
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)[kernel]
+            d = json.load(f)[kernel][workload]
     except Exception:
         return None
     if d.get("source_sha256") != source_hash(kernel) or d.get("workload") != workload:
