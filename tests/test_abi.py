@@ -96,6 +96,15 @@ def test_debug_knob_validation(lib):
     assert lib.fa_debug_inject(7) == -8
     assert lib.fa_debug_inject(0) == 0
     assert lib.fa_debug_set_wait_timeout_ns(2_000_000_000) == 0
+    assert lib.fa_set_deterministic(2) == -8
+    assert lib.fa_set_deterministic(0) == 0
+
+
+def test_backward_plan_query_argument_errors(lib):
+    # host-only: sizes are checked before the device is looked at
+    assert lib.fa_bwd_sums_dq_in_place(0, 1, 128, 64) == -2
+    assert lib.fa_bwd_sums_dq_in_place(1, 1, 0, 64) == -2
+    assert lib.fa_bwd_sums_dq_in_place(1, 1, 128, 96) == -3
 
 
 def test_argument_errors_decode(lib):
