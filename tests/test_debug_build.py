@@ -121,3 +121,32 @@ def test_debug_build_grouped_and_packed_clean(dlib, causal):
     o_ref, _ = oracle.attn_fwd_varlen(to_f64(qp.cpu()), to_f64(kp.cpu()), to_f64(vp_.cpu()), cu.cpu().numpy(), scale,
                                       causal)
     assert o_ok(to_f64(op.cpu()), o_ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["causal_b4h16t2048d64", "causal_b2h16t8192d128", "ragged_b8h32t3000d128"])
+def test_debug_build_full_size_workloads_clean(dlib, name):
+    # every run-time index of the full-size launches (the configurations the
+    # bench times) passes its check, and the debug build computes the product
+    # build's bits
+    from online_softmax_05_gb300.inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS[name]
+    causal = int(w.causal[0])
+    dev = torch.device("cuda")
+    q, k, v, do = (t.to(dev) for t in workload_inputs(w))
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    B, H, T, D = w.B, w.H, w.T, w.D
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, T, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    assert dlib.fa_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, T, D, w.scale, causal, stream) == 0
+    assert dlib.fa_bwd(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv), B, H, T, D, w.scale,
+                       causal, stream) == 0
+    assert dlib.fa_get_device_status(stream) == 0
+    o2, lse2 = fa.attention_forward(q, k, v, causal=bool(causal), scale=w.scale)
+    g2 = fa.attention_backward(q, k, v, o, lse, do, causal=bool(causal), scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    assert same_gradients((dq, dk, dv), g2, D)
