@@ -5,8 +5,9 @@
 // "Output and saved state").
 //
 // One persistent CTA per SM walks work items (pair of 128-row query tiles,
-// batch*head; a single query tile when there are too few pairs to fill half
-// the SMs).  Warp roles:
+// batch*head; when there are too few pairs to fill half the SMs, a single
+// query tile whose key tiles the two softmax warpgroups split, their running
+// states merged at the end).  Warp roles:
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one query row each)
 //   warps 4-7  softmax for query tile 1
 //   warp 8     TMA producer: Q tiles once per item, K/V tiles into a ring
@@ -55,9 +56,11 @@ struct FwdCfg {
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
     // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] epi[2] mma_done
-    // ph_full[2]
-    static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1 + 2;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    // ph_full[2] mrg_full mrg_done
+    static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1 + 2 + 2;
+    // split items: the second warpgroup's row max and row sum, 2 x 128 floats
+    static constexpr int kMrgOff = kBarOff + kNumBars * 8;
+    static constexpr int kMiscOff = kMrgOff + 2 * 128 * 4;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + tmem slot, abort flag, alignment slack
     // TMEM columns (512 allocated): S0, S1 (P aliases their first 64 columns), O0, O1
     __device__ static constexpr uint32_t kS(int t) { return 128u * t; }
@@ -78,7 +81,8 @@ struct FwdParams {
     __nv_bfloat16* o_packed;  // O of the packed layout (stored row by row, not by TMA)
     int head_pairs;       // 1: the two query tiles of an item are two heads of one group at the same rows
     int n_tiles;          // query tiles per head
-    int single_tiles;     // 1: an item is one query tile (few items: each gets an SM of its own)
+    int single_tiles;     // 1: an item is one query tile whose key tiles the two softmax warpgroups split
+                          // (few items: each gets an SM of its own)
     int head_major;       // 1: items of one head are consecutive (no causal masking: every item weighs the
                           // same, so the CTAs in flight share few heads' K/V tiles in L2)
     float sl2_eff;  // multiplier applied inside exp2: scale*log2e, or 1 when prescaled
@@ -181,11 +185,10 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
         // (query tile, head), heaviest tiles first; the second half is empty
         const int t = p.head_major ? w % p.n_tiles : p.n_tiles - 1 - w / p.BH;
         const int bh = p.head_major ? w / p.n_tiles : w % p.BH;
-        it.tile[0] = t;
-        it.tile[1] = p.n_tiles;  // past T: the second warpgroup skips the item
+        it.tile[0] = it.tile[1] = t;  // the second warpgroup takes the second half of the key tiles
         it.bh[0] = it.bh[1] = bh;
         it.bh_kv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
-        it.valid1 = false;
+        it.valid1 = false;  // no second Q tile
     } else if (p.head_pairs) {
         const int per_t = p.BH / 2;  // head pairs over all batches
         const int t = p.head_major ? w % p.n_tiles : p.n_tiles - 1 - w / per_t;
@@ -216,7 +219,10 @@ __device__ __forceinline__ int item_of(int k, int n_items) {
     return w < n_items ? w : -1;
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+// SPLIT: every item is one query tile whose key tiles the two softmax
+// warpgroups split (launched when the items are too few to fill the SMs);
+// compiled apart so the paired kernel carries none of it.
+template <int D, bool CAUSAL, bool VARLEN, bool SPLIT>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdParams p) {
@@ -238,6 +244,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t mma_done = bars + 8u * (12 + 2 * C::kStages);
     // ph_full(t): the first half of P (keys 0..63) and the O rescale are done
     auto ph_full = [&](int t) { return bars + 8u * (13 + 2 * C::kStages + t); };
+    // split items: the second warpgroup published its row max and sum, its O is complete
+    // (4 warps) / the first warpgroup has read them and that O (4 warps)
+    const uint32_t mrg_full = bars + 8u * (15 + 2 * C::kStages), mrg_done = bars + 8u * (16 + 2 * C::kStages);
+    float* mrg = reinterpret_cast<float*>(smem + C::kMrgOff);  // [0][row] max (log2 units), [1][row] sum
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
     const Ctl ctl{abort_flag, p.timeout_ns};
@@ -259,6 +269,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(kv_empty(s), 1);
         }
         mbar_init(mma_done, 1);
+        mbar_init(mrg_full, 4);
+        mbar_init(mrg_done, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -306,31 +318,50 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         tma_load_3d_hint(sQ[t] + a * C::kAtomBytes, &tm_q, q_full(t), 64 * a,
                                          VARLEN ? item.bh[t] : qrow, VARLEN ? qrow : item.bh[t], pol_q);
                 }
-                for (int j = 0; j < nmax; ++j) {
-                    for (int kind = 0; kind < 2; ++kind) {
-                        const uint32_t slot = kv_cnt % C::kStages;
-                        if (!wait_bar(kv_empty(slot), ((kv_cnt / C::kStages) & 1) ^ 1, ctl)) goto producer_done;
-                        ++kv_cnt;
-                        if (skip_first) {  // test hook: never deliver this tile
-                            skip_first = false;
-                            skipped_fill = static_cast<int>(kv_cnt - 1);
-                            continue;
-                        }
-                        const int krow = item.row0 + j * kBN;
-                        // the key tile is one this query tile needs, inside the tensor, and its ring
-                        // stage lies inside the shared-memory window
-                        if (!FA_CHECK(j * kBN < item.T && bh >= 0 && bh < p.BH / p.group &&
-                                          C::kKVOff + (slot + 1) * C::kTileBytes <= C::kBarOff,
-                                      &g_status_fwd, abort_flag)) {
-                            --kv_cnt;  // nothing was armed: the drain must not wait for this fill
-                            goto producer_done;
-                        }
-                        mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
-                        const CUtensorMap* tm = kind ? &tm_v : &tm_k;
-                        for (int a = 0; a < C::kAtoms; ++a)
-                            tma_load_3d_hint(sKV + slot * C::kTileBytes + a * C::kAtomBytes, tm, kv_full(slot),
-                                             64 * a, VARLEN ? bh : krow, VARLEN ? krow : bh, pol_kv);
+                // one K (kind 0) or V (kind 1) tile into the next ring stage
+                auto fill = [&](int kind, int jt) -> bool {
+                    const uint32_t slot = kv_cnt % C::kStages;
+                    if (!wait_bar(kv_empty(slot), ((kv_cnt / C::kStages) & 1) ^ 1, ctl)) return false;
+                    ++kv_cnt;
+                    if (skip_first) {  // test hook: never deliver this tile
+                        skip_first = false;
+                        skipped_fill = static_cast<int>(kv_cnt - 1);
+                        return true;
                     }
+                    const int krow = item.row0 + jt * kBN;
+                    // the key tile is one this query tile needs, inside the tensor, and its ring
+                    // stage lies inside the shared-memory window
+                    if (!FA_CHECK(jt * kBN < item.T && bh >= 0 && bh < p.BH / p.group &&
+                                      C::kKVOff + (slot + 1) * C::kTileBytes <= C::kBarOff,
+                                  &g_status_fwd, abort_flag)) {
+                        --kv_cnt;  // nothing was armed: the drain must not wait for this fill
+                        return false;
+                    }
+                    mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
+                    const CUtensorMap* tm = kind ? &tm_v : &tm_k;
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_3d_hint(sKV + slot * C::kTileBytes + a * C::kAtomBytes, tm, kv_full(slot), 64 * a,
+                                         VARLEN ? bh : krow, VARLEN ? krow : bh, pol_kv);
+                    return true;
+                };
+                if constexpr (SPLIT) {
+                    // split item: warpgroup 0 takes key tiles 0 .. h-1, warpgroup 1 h .. n0-1,
+                    // filled in the order the MMA warp consumes them
+                    const int h = (n0 + 1) / 2, m1 = n0 - h;
+                    if (!fill(0, 0)) goto producer_done;
+                    if (m1 > 0 && !fill(0, h)) goto producer_done;
+                    for (int j = 0; j < h; ++j) {
+                        if (!fill(1, j)) goto producer_done;
+                        if (j + 1 < h && !fill(0, j + 1)) goto producer_done;
+                        if (j < m1) {
+                            if (!fill(1, h + j)) goto producer_done;
+                            if (j + 1 < m1 && !fill(0, h + j + 1)) goto producer_done;
+                        }
+                    }
+                } else {
+                    for (int j = 0; j < nmax; ++j)
+                        for (int kind = 0; kind < 2; ++kind)
+                            if (!fill(kind, j)) goto producer_done;
                 }
             }
         producer_done:
@@ -356,10 +387,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const SDesc dKV_km = sdesc_make(sKV, 16, 1024);
             const SDesc dKV_mn = sdesc_make(sKV, C::kAtomBytes, 1024);
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
-            auto issue_s = [&](int t, uint32_t slot) {
-                if (!FA_CHECK(t >= 0 && t < 2 && slot < C::kStages && C::kS(t) + 128 <= 512u, &g_status_fwd, abort_flag))
+            // S_t = Q K^T into S buffer t, Q from Q buffer qb (split items: both use buffer 0)
+            auto issue_s = [&](int t, uint32_t slot, int qb) {
+                if (!FA_CHECK(t >= 0 && t < 2 && qb >= 0 && qb < 2 && slot < C::kStages && C::kS(t) + 128 <= 512u,
+                              &g_status_fwd, abort_flag))
                     return;
-                const uint32_t qo = t * kTile16, ko = slot * kTile16;
+                const uint32_t qo = qb * kTile16, ko = slot * kTile16;
 #pragma unroll
                 for (int s = 0; s < D / 16; ++s) {
                     const uint32_t off = ((s >> 2) * C::kAtomBytes + (s & 3) * 32) >> 4;
@@ -391,15 +424,65 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     if (!wait_all(q_full(1), q_cnt[1] & 1, ctl)) goto mma_done_label;
                     ++q_cnt[1];
                 }
+                if constexpr (SPLIT) {
+                    // Split item: one query tile (Q buffer 0); S buffer / warpgroup 0 takes key
+                    // tiles 0 .. h-1, S buffer / warpgroup 1 takes h .. n0-1, each with its own K
+                    // and V tiles, in the order the producer fills them.
+                    const int h = (n0 + 1) / 2, cnt[2] = {h, n0 - h};
+                    auto next_slot = [&](uint32_t& slot) -> bool {
+                        slot = kv_cnt % C::kStages;
+                        if (!wait_all(kv_full(slot), (kv_cnt / C::kStages) & 1, ctl)) return false;
+                        ++kv_cnt;
+                        tc_fence_after();
+                        return true;
+                    };
+                    for (int t = 0; t < 2; ++t) {
+                        if (cnt[t] == 0) continue;
+                        uint32_t ks;
+                        if (!next_slot(ks)) goto mma_done_label;
+                        issue_s(t, ks, 0);
+                        if (leader) {
+                            mma_commit(s_full(t));
+                            mma_commit(kv_empty(ks));
+                        }
+                    }
+                    for (int j = 0; j < h; ++j) {
+                        for (int t = 0; t < 2; ++t) {
+                            if (j >= cnt[t]) continue;
+                            uint32_t vs;
+                            if (!next_slot(vs)) goto mma_done_label;
+                            if (!wait_all(ph_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
+                            tc_fence_after();
+                            issue_pv_half(t, vs, j > 0, 0);
+                            if (!wait_all(p_full(t), p_cnt[t] & 1, ctl)) goto mma_done_label;
+                            ++p_cnt[t];
+                            tc_fence_after();
+                            issue_pv_half(t, vs, true, 1);
+                            if (leader) mma_commit(kv_empty(vs));
+                            if (j + 1 < cnt[t]) {
+                                uint32_t ks;
+                                if (!next_slot(ks)) goto mma_done_label;
+                                issue_s(t, ks, 0);
+                                if (leader) {
+                                    mma_commit(s_full(t));
+                                    mma_commit(kv_empty(ks));
+                                }
+                            } else {
+                                if (leader) mma_commit(o_full(t));
+                            }
+                        }
+                    }
+                    continue;
+                }
                 {
                     const uint32_t ks = kv_cnt % C::kStages;
                     if (!wait_all(kv_full(ks), (kv_cnt / C::kStages) & 1, ctl)) goto mma_done_label;
                     ++kv_cnt;
                     tc_fence_after();
-                    issue_s(0, ks);
+                    issue_s(0, ks, 0);
                     if (leader) mma_commit(s_full(0));
                     if (n1 > 0) {
-                        issue_s(1, ks);
+                        issue_s(1, ks, 1);
                         if (leader) mma_commit(s_full(1));
                     }
                     if (leader) mma_commit(kv_empty(ks));
@@ -429,7 +512,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                 tc_fence_after();
                                 k_ready = true;
                             }
-                            issue_s(t, ks);
+                            issue_s(t, ks, t);
                             if (leader) mma_commit(s_full(t));
                         } else {
                             if (leader) mma_commit(o_full(t));
@@ -462,8 +545,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int r_local = 32 * wq + lane;
         const uint32_t lane_base = tmem + ((32u * wq) << 16);
         const uint32_t tS = lane_base + C::kS(t), tO = lane_base + C::kO(t);
-        uint32_t s_cnt = 0, o_cnt = 0, epi_cnt = 0;
+        uint32_t s_cnt = 0, o_cnt = 0, epi_cnt = 0, mrg_cnt = 0;
         const float eff = p.sl2_eff;
+        constexpr bool split = SPLIT;
         if (!FA_CHECK(t < 2 && C::kS(t) + 128 <= 512u && C::kO(t) + D <= 512u, &g_status_fwd, abort_flag))
             goto softmax_done;
         for (int k = 0;; ++k) {
@@ -473,9 +557,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int tile = item.tile[t], bh = item.bh[t], T = item.T;
             if (tile * kFwdBM >= T) continue;  // the second tile of an item may be empty (or the whole item)
             const int row = tile * kFwdBM + r_local;  // row within the sequence
-            const int n = fwd_num_kv_tiles(T, CAUSAL, tile);
+            const int n_all = fwd_num_kv_tiles(T, CAUSAL, tile);
+            // split item: this warpgroup's share of the key tiles (the first half, rounded up,
+            // for warpgroup 0); otherwise all of them
+            const int h_split = (n_all + 1) / 2;
+            const int j_off = (split && t == 1) ? h_split : 0;
+            const int n = split ? (t == 0 ? h_split : n_all - h_split) : n_all;
             float m_used = -INFINITY, l = 0.f;
-            for (int j = 0; j < n; ++j) {
+            for (int jj = 0; jj < n; ++jj) {
+                const int j = jj + j_off;  // key tile
                 if (!warp_wait<false>(s_full(t), s_cnt & 1, ctl)) goto softmax_done;
                 ++s_cnt;
                 tc_fence_after();
@@ -514,7 +604,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const float m_new = fmaxf(m_used, m_tile);
                 float alpha = 1.f;
                 bool need = false;
-                if (j == 0) {
+                if (jj == 0) {
                     m_used = m_new;
                 } else if (m_new > m_used + kRescaleThreshold) {
                     need = true;
@@ -584,9 +674,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(t));
             }
-            // ---- epilogue: O = acc / l through shared memory and a TMA store; LSE per row
+            // ---- split item: warpgroup 1 hands its row state to warpgroup 0 and waits until its O
+            // has been read; warpgroup 0 merges the two halves with the online-softmax rule
+            // ("Lab 06", section 2: state from disjoint key ranges combines by rescaling)
+            float a0 = 1.f, a1 = 0.f;
+            const bool has1 = split && (n_all - h_split) > 0;
+            if (split && t == 1) {
+                if (n > 0) {
+                    if (!warp_wait(o_full(1), o_cnt & 1, ctl)) goto softmax_done;
+                    ++o_cnt;
+                }
+                mrg[r_local] = n > 0 ? m_used : -INFINITY;
+                mrg[128 + r_local] = n > 0 ? l : 0.f;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(mrg_full);
+                if (!warp_wait(mrg_done, mrg_cnt & 1, ctl)) goto softmax_done;
+                ++mrg_cnt;
+                continue;
+            }
             if (!warp_wait(o_full(t), o_cnt & 1, ctl)) goto softmax_done;
             ++o_cnt;
+            if (split) {
+                if (!warp_wait(mrg_full, mrg_cnt & 1, ctl)) goto softmax_done;
+                ++mrg_cnt;
+                const float m1 = reinterpret_cast<volatile float*>(mrg)[r_local];
+                const float l1 = reinterpret_cast<volatile float*>(mrg)[128 + r_local];
+                if (has1) {
+                    const float mm = fmaxf(m_used, m1);
+                    a0 = ex2_approx(m_used - mm);
+                    a1 = ex2_approx(m1 - mm);
+                    l = l * a0 + l1 * a1;
+                    m_used = mm;
+                }
+            }
             tc_fence_after();
             if constexpr (VARLEN) {
                 // packed rows past this sequence's end belong to the next one: store row by row
@@ -622,12 +742,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     p.lse[static_cast<size_t>(bh) * p.total + item.row0 + row] = (m_used + __log2f(l)) * kLn2;
             } else {
                 const float inv = 1.f / l;
+                const uint32_t tO1 = lane_base + C::kO(1);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t orr[32];
                     tmem_ld32(tO + 32 * c, orr);
-                    tmem_ld_wait();
-                    reg_fence32(orr);
+                    if (has1) {
+                        uint32_t o1[32];
+                        tmem_ld32(tO1 + 32 * c, o1);
+                        tmem_ld_wait();
+                        reg_fence32(orr);
+                        reg_fence32(o1);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            orr[e] = __float_as_uint(fmaf(__uint_as_float(orr[e]), a0, __uint_as_float(o1[e]) * a1));
+                    } else {
+                        tmem_ld_wait();
+                        reg_fence32(orr);
+                    }
                     const int col0 = 32 * c;
                     const uint32_t atom = sQ[t] + (col0 >> 6) * C::kAtomBytes;
 #pragma unroll
@@ -644,6 +776,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
+                if (split && lane == 0) mbar_arrive(mrg_done);  // warpgroup 1's O has been read
                 if (lane == 0) mbar_arrive(epi_bar(t));
                 if (wq == 0 && lane == 0) {
                     if (wait_bar(epi_bar(t), epi_cnt & 1, ctl) &&
@@ -672,11 +805,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
-template <int D, bool CAUSAL, bool VARLEN = false>
+template <int D, bool CAUSAL, bool VARLEN = false, bool SPLIT = false>
 int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                  const FwdParams& p, int grid, cudaStream_t st) {
     static bool attr_set = false;
-    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, SPLIT>;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmemBytes) !=
             cudaSuccess)
@@ -729,12 +862,20 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
     if (dbg.ev[0]) cudaEventRecord(dbg.ev[0], stream);
     int rc;
-    if (D == 64)
+    if (p.single_tiles) {
+        if (D == 64)
+            rc = causal ? launch_fwd_t<64, true, false, true>(tq, tk, tv, to, p, grid, stream)
+                        : launch_fwd_t<64, false, false, true>(tq, tk, tv, to, p, grid, stream);
+        else
+            rc = causal ? launch_fwd_t<128, true, false, true>(tq, tk, tv, to, p, grid, stream)
+                        : launch_fwd_t<128, false, false, true>(tq, tk, tv, to, p, grid, stream);
+    } else if (D == 64) {
         rc = causal ? launch_fwd_t<64, true>(tq, tk, tv, to, p, grid, stream)
                     : launch_fwd_t<64, false>(tq, tk, tv, to, p, grid, stream);
-    else
+    } else {
         rc = causal ? launch_fwd_t<128, true>(tq, tk, tv, to, p, grid, stream)
                     : launch_fwd_t<128, false>(tq, tk, tv, to, p, grid, stream);
+    }
     if (dbg.ev[1]) cudaEventRecord(dbg.ev[1], stream);
     return rc;
 }

@@ -117,11 +117,12 @@ def test_forward_workload_full_compare(name):
 @pytest.mark.gpu
 @pytest.mark.parametrize("D,T", [(64, 1024), (128, 2048), (128, 1000)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_work_partition_does_not_change_bits(D, T, causal):
+def test_work_partition_keeps_parity(D, T, causal):
     # One batch of 4 heads has few work items, so each query tile gets an SM of
-    # its own; inside a batch of 16 x 8 heads the same heads are walked as pairs
-    # of query tiles by persistent CTAs.  Every row's arithmetic is the same in
-    # both, so the outputs of the shared heads must agree bit for bit.
+    # its own and its two softmax warpgroups split the key tiles (their states
+    # merged at the end); inside a batch of 16 x 4 heads the same heads are
+    # walked as pairs of query tiles by persistent CTAs.  Both must match the
+    # oracle on the shared heads, and agree with each other to rounding.
     H = 4
     q, k, v, _ = make_inputs(16, H, T, D, seed=21)
     dev = torch.device("cuda")
@@ -130,5 +131,9 @@ def test_work_partition_does_not_change_bits(D, T, causal):
     o_big, l_big = fa.attention_forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == 0
-    assert torch.equal(o_small[0], o_big[0])
-    assert torch.equal(l_small[0], l_big[0])
+    o_ref, lse_ref = oracle.attn_fwd(to_f64(q[0]), to_f64(k[0]), to_f64(v[0]), scale, causal)
+    for o, lse in ((o_small[0], l_small[0]), (o_big[0], l_big[0])):
+        assert o_ok(to_f64(o.cpu()), o_ref)
+        assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= LSE_TOL
+    assert (o_small[0].float() - o_big[0].float()).abs().max().item() <= 2 ** -5
+

@@ -105,8 +105,16 @@ def test_single_sequence_equals_dense_forward(causal):
     ld = torch.empty(1, H, T, device=dev)
     assert fa.fa_fwd(qd, kd, vd, od, ld, 1, H, T, D, 0.09, int(causal), torch.cuda.current_stream()) == 0
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(o, to_f64(od[0].permute(1, 0, 2).cpu()))
-    np.testing.assert_array_equal(lse, ld[0].cpu().double().numpy())
+    # The packed forward walks pairs of query tiles; the dense call on one head
+    # group this small gives each query tile an SM and splits its key tiles
+    # between the two softmax warpgroups, so the two agree to rounding (and each
+    # matches the oracle)
+    od = to_f64(od[0].permute(1, 0, 2).cpu())
+    ld = ld[0].cpu().double().numpy()
+    o_ref, lse_ref = oracle.attn_fwd_varlen(to_f64(q), to_f64(k), to_f64(v), cu, 0.09, causal)
+    assert o_ok(o, o_ref) and o_ok(od, o_ref)
+    assert np.abs(lse - lse_ref).max() <= LSE_TOL and np.abs(ld - lse_ref).max() <= LSE_TOL
+    assert np.abs(o - od).max() <= 2 ** -5 and np.abs(lse - ld).max() <= 1e-5
 
 
 @pytest.mark.gpu
@@ -213,8 +221,13 @@ def test_varlen_backward_single_sequence_equals_dense(causal):
     o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=0.09)
     dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=0.09)
     torch.cuda.synchronize()
+    # the dense forward of this small head group splits each query tile's key
+    # tiles between two warpgroups, so its O and LSE (the backward's inputs)
+    # differ from the packed forward's in rounding: the gradients agree within
+    # the gradient tolerance
     for g, d in zip(got, (dq, dk, dv)):
-        np.testing.assert_array_equal(g, to_f64(d[0].permute(1, 0, 2).cpu()))
+        d = to_f64(d[0].permute(1, 0, 2).cpu())
+        assert np.abs(g - d).max() <= grad_bound(d)
 
 
 @pytest.mark.gpu
