@@ -286,9 +286,12 @@ def algorithmic_bytes(B, H, T, D, bwd):
 def run_configs(args):
     """Every specified workload, forward and (where specified) backward: median
     over at least 20 launches after 5 warm-ups, each between its own pair of
-    events.  The small
-    non-causal forward (B=1 H=8 T=1024 D=64) is also timed with a 256 MB write
-    between launches, so it starts with a cold L2.  One JSON line per case."""
+    events (`ms`), and the mean over the same number of launches between one
+    pair of events (`ms_back_to_back`; the launches' fixed GPU-side costs then
+    overlap).  The small non-causal forward (B=1 H=8 T=1024 D=64) is also
+    timed with a 256 MB write between launches, so it starts with a cold L2.
+    One JSON line per case, then one with the event-pair time of a one-element
+    torch kernel: the floor of the per-launch method on this GPU."""
     import torch
     import online_softmax_05_gb300 as fa
     from online_softmax_05_gb300.inputs import WORKLOADS, workload_inputs
@@ -317,8 +320,8 @@ def run_configs(args):
                 for _ in range(max(5, args.warmup)):
                     assert fn() == 0
                 torch.cuda.synchronize(dev)
-                # all launches enqueued back to back with an event pair around each,
-                # so host-side launch work is hidden and each pair times the GPU only
+                # all launches enqueued back to back with an event pair around each:
+                # host-side launch work is hidden, each pair times one launch on the GPU
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(n_iter)]
                 for e0, e1 in evs:
@@ -331,6 +334,15 @@ def run_configs(args):
                 times = [e0.elapsed_time(e1) for e0, e1 in evs]
                 assert fa.fa_get_device_status(stream) == 0
                 ms = sorted(times)[len(times) // 2]
+                ms_b2b = None
+                if not flush:
+                    e0, e1 = evs[0]
+                    e0.record(stream)
+                    for _ in range(n_iter):
+                        fn()
+                    e1.record(stream)
+                    torch.cuda.synchronize(dev)
+                    ms_b2b = e0.elapsed_time(e1) / n_iter
                 bwd = pname == "bwd"
                 fl = fwd_fl * (2.5 if bwd else 1.0)
                 nbytes = algorithmic_bytes(B, H, T, D, bwd)
@@ -338,7 +350,7 @@ def run_configs(args):
                         "B": B, "H": H, "T": T, "D": D, "ms": ms, "tflops": fl / ms / 1e9,
                         "frac_of_burst": fl / ms / 1e9 / peaks["bf16_tflops"], "gbs": nbytes / ms / 1e6,
                         "frac_of_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"], "iters": n_iter,
-                        "peaks": src, "dtype": "bf16", "data": "synthetic"}
+                        "ms_back_to_back": ms_b2b, "peaks": src, "dtype": "bf16", "data": "synthetic"}
                 if bwd:
                     # the backward's two main kernels, timed apart in a pass of their own
                     # (events between them serialise the grids, which otherwise overlap)
@@ -356,6 +368,16 @@ def run_configs(args):
                     line["dkdv_ms"] = med([e[0].elapsed_time(e[1]) for e in kev])
                     line["dq_ms"] = med([e[1].elapsed_time(e[2]) for e in kev])
                 print(json.dumps(line), flush=True)
+    # the per-launch method's own floor: a one-element torch kernel between an event pair
+    x = torch.zeros(1, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_iter)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        x.add_(1)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    floor = sorted(e0.elapsed_time(e1) for e0, e1 in evs)[n_iter // 2]
+    print(json.dumps({"harness": "event pair around one one-element torch kernel", "ms": floor}), flush=True)
 
 
 def run_sweep(args):
