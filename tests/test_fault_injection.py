@@ -1,7 +1,8 @@
 """Failure detection without a GPU fault: every in-kernel wait is bounded.
 
 A host-side test hook tells one kernel's load warp to skip one tile copy:
-  mode 1  the forward's load warp, its first K/V copy;
+  mode 1  the forward's load warp, its first K/V copy (a small grid's split
+          items and a full grid's pairs of query tiles);
   mode 2  the first dK/dV CTA of the backward, its third Q copy (at D = 64
           on a full grid that CTA also sums dQ, so reduce-adds are in flight);
   mode 3  the first dQ CTA of the backward, its first K copy.
@@ -42,8 +43,11 @@ def _inject(lib, mode, fn):
 
 
 @pytest.mark.gpu
-def test_skipped_copy_reports_timeout_and_recovers(lib):
-    B, H, T, D = 1, 2, 300, 64
+@pytest.mark.parametrize("B,H,T", [(1, 2, 300), (4, 16, 1280)], ids=["split_items", "paired_items"])
+def test_skipped_copy_reports_timeout_and_recovers(lib, B, H, T):
+    # a small grid runs one query tile per item, its key tiles split between the
+    # two softmax warpgroups; a full grid runs pairs of query tiles
+    D = 64
     q, k, v, _ = make_inputs(B, H, T, D, seed=1)
     dev = torch.device("cuda")
     qd, kd, vd = (t.to(dev) for t in (q, k, v))
@@ -60,9 +64,10 @@ def test_skipped_copy_reports_timeout_and_recovers(lib):
     o2, lse2 = fa.attention_forward(qd, kd, vd, causal=False)
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == 0
-    o_ref, lse_ref = oracle.attn_fwd(to_f64(q), to_f64(k), to_f64(v), 1 / math.sqrt(D), False)
-    assert o_ok(to_f64(o2.cpu()), o_ref)
-    assert np.abs(lse2.cpu().double().numpy() - lse_ref).max() <= 1e-3
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        o_ref, lse_ref = oracle.attn_fwd(to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h]), 1 / math.sqrt(D), False)
+        assert o_ok(to_f64(o2[b, h].cpu()), o_ref)
+        assert np.abs(lse2[b, h].cpu().double().numpy() - lse_ref).max() <= 1e-3
 
 
 @pytest.mark.gpu
