@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import datetime
 import hashlib
+import re
 import json
 import math
 import os
@@ -117,11 +118,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_only(text):
+    """Source text without comments and with whitespace collapsed: what the
+    compiler sees, so that a comment edit does not void a measurement."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return " ".join(text.split())
+
+
 def source_hash(kernel):
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel] + COMMON_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()
 
 

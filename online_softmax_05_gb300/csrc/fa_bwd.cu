@@ -27,6 +27,12 @@
 //                recomputed (S = Q K^T, dP = dO V^T), dS goes to TMEM as bf16
 //                and dQ += dS K; dQ*scale leaves once, in bf16.
 // The two main kernels read the same inputs and write disjoint outputs.
+// At D = 64, on grids of at least one dK/dV CTA per SM, the backward keeps
+// section 4's own loop order instead: fa_bwd_dkdv (FUSE) also computes each
+// query tile's dS K and adds it into an fp32 dQ accumulator with TMA
+// reduce-adds (zeroed by fa_bwd_pre), and fa_bwd_dq_convert writes dQ*scale
+// in bf16.  The sum order of those adds varies from run to run;
+// fa_set_deterministic(1) selects the two-kernel form.
 #include <cuda_runtime.h>
 
 #include <mutex>
