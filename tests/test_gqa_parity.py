@@ -110,3 +110,29 @@ def test_gqa_fused_backward_full_grid(causal):
         rq, rk, rv, _ = oracle.attn_bwd_gqa(qf, kf, vf, df, scale, causal)
         for name, g, r in (("dq", dq[b:b + 1], rq), ("dk", dk[b:b + 1], rk), ("dv", dv[b:b + 1], rv)):
             assert np.abs(g - r).max() <= grad_bound(r), (name, b)
+
+
+@pytest.mark.gpu
+@pytest.mark.slow
+def test_gqa_long_context_whole_groups():
+    # The long-context causal shape with 4 query heads per K/V head (B=2,
+    # Hq=16, Hkv=4, T=8192, D=128) at full size.  Two whole groups are compared
+    # element by element: K/V head 0 of batch 0 and K/V head 3 of batch 1, with
+    # their 4 query heads each (O, LSE, dQ of the query heads; dK, dV summed
+    # over the group).
+    B, Hq, Hkv, T, D = 2, 16, 4, 8192, 128
+    q, k, v, do = make(B, Hq, Hkv, T, D, seed=13)
+    scale = D ** -0.5
+    o, dq, dk, dv, lse = run(q, k, v, do, True, scale)
+    g = Hq // Hkv
+    for b, kvh in ((0, 0), (1, Hkv - 1)):
+        hs = slice(kvh * g, (kvh + 1) * g)
+        qf, df = (to_f64(t[b:b + 1, hs]) for t in (q, do))
+        kf, vf = (to_f64(t[b:b + 1, kvh:kvh + 1]) for t in (k, v))
+        o_ref, lse_ref = oracle.attn_fwd_gqa(qf, kf, vf, scale, True)
+        assert o_ok(o[b:b + 1, hs], o_ref), (b, kvh)
+        assert np.abs(lse[b:b + 1, hs] - lse_ref).max() <= LSE_TOL, (b, kvh)
+        rq, rk, rv, _ = oracle.attn_bwd_gqa(qf, kf, vf, df, scale, True)
+        for name, got, r in (("dq", dq[b:b + 1, hs], rq), ("dk", dk[b:b + 1, kvh:kvh + 1], rk),
+                             ("dv", dv[b:b + 1, kvh:kvh + 1], rv)):
+            assert np.abs(got - r).max() <= grad_bound(r), (name, b, kvh)

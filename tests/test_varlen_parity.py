@@ -277,3 +277,32 @@ def test_varlen_backward_serving_mix_sampled_rows(causal):
                                                     rows, rows)
             for name, g, r in (("dq", dq[a + rows, h], rq), ("dk", dk[a + rows, h], rk), ("dv", dv[a + rows, h], rv)):
                 assert np.abs(g - r).max() <= grad_bound(r), (name, s, h)
+
+
+@pytest.mark.gpu
+@pytest.mark.slow
+def test_serving_pack_whole_sequences():
+    # The packed batch the bench times: 48 causal requests of 128..8192 tokens
+    # (numpy seed 0), 16 heads, D = 128, inputs seed 0.  Forward and backward
+    # run on the whole pack; the longest, the shortest and the median-length
+    # request are compared against the oracle in full, every head and row.
+    n_seq, H, D = 48, 16, 128
+    lengths = np.random.default_rng(0).integers(128, 8193, size=n_seq)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    total, Tmax = int(cu[-1]), int(lengths.max())
+    g = torch.Generator().manual_seed(0)
+    q, k, v, do = (torch.randn(total, H, D, generator=g).to(torch.bfloat16) for _ in range(4))
+    scale = D ** -0.5
+    o, lse = run(q, k, v, cu, Tmax, True, scale)
+    dq, dk, dv = run_bwd(q, k, v, do, cu, Tmax, True, scale)
+    order = np.argsort(lengths, kind="stable")
+    for s in (int(order[-1]), int(order[0]), int(order[n_seq // 2])):
+        a, L = int(cu[s]), int(lengths[s])
+        sl = slice(a, a + L)
+        # (L, H, D) -> (1, H, L, D) for the dense oracle
+        qf, kf, vf, df = (to_f64(t[sl]).transpose(1, 0, 2)[None] for t in (q, k, v, do))
+        o_ref, lse_ref = oracle.attn_fwd(qf, kf, vf, scale, True)
+        assert o_ok(o[sl].transpose(1, 0, 2)[None], o_ref), s
+        assert np.abs(lse[:, sl][None] - lse_ref).max() <= LSE_TOL, s
+        ref = oracle.attn_bwd(qf, kf, vf, df, scale, True)[:3]
+        check_grads([t[sl].transpose(1, 0, 2)[None] for t in (dq, dk, dv)], ref)
