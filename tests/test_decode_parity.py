@@ -91,3 +91,22 @@ def test_decode_equals_forward_when_lengths_match():
     torch.cuda.synchronize()
     assert np.abs(o_dec - to_f64(o_fwd.cpu())).max() <= 1e-2
     assert np.abs(lse_dec - lse_fwd.cpu().double().numpy()).max() <= 1e-3
+
+
+@pytest.mark.gpu
+@pytest.mark.slow
+def test_decode_bench_shape_every_head():
+    # the shape the bench times: one new token for each of B=8 x H=32 heads
+    # against a 32768-token cache, D = 128 (its own split of the keys across
+    # CTAs); every head compared, 32 heads at a time on the host
+    B, H, Tq, Tk, D = 8, 32, 1, 32768, 128
+    q, k, v = make(B, H, Tq, Tk, D, seed=8)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run(q, k, v, scale)
+    q3, k3, v3 = (t.reshape(B * H, 1, -1, D) for t in (q, k, v))
+    o3, lse3 = o.reshape(B * H, 1, Tq, D), lse.reshape(B * H, 1, Tq)
+    for lo in range(0, B * H, 32):
+        hs = slice(lo, lo + 32)
+        o_ref, lse_ref = oracle.attn_fwd_cross(to_f64(q3[hs]), to_f64(k3[hs]), to_f64(v3[hs]), scale)
+        assert o_ok(o3[hs], o_ref), lo
+        assert np.abs(lse3[hs] - lse_ref).max() <= LSE_TOL, lo
