@@ -131,11 +131,12 @@ def test_work_partition_does_not_change_bits_backward(D, causal, deterministic_b
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
-def test_long_sequence_sampled_rows(D, causal):
-    # one head of 32731 tokens (256 tiles, the last one ragged): forward O and
-    # LSE and backward dQ, dK, dV on sampled rows, including both ends
-    T = 32768 - 37
+@pytest.mark.parametrize("D,causal,T", [(128, True, 32768 - 37), (64, False, 32768 - 37),
+                                         pytest.param(128, True, 65536 + 61, marks=pytest.mark.slow)])
+def test_long_sequence_sampled_rows(D, causal, T):
+    # one head of 32731 tokens (256 tiles, the last one ragged), or of 65597
+    # (513 tiles, the last one holding 61 rows): forward O and LSE and
+    # backward dQ, dK, dV on sampled rows, including both ends
     q, k, v, do = make_inputs(1, 1, T, D, seed=41)
     scale = D ** -0.5
     dev = torch.device("cuda")
@@ -145,7 +146,8 @@ def test_long_sequence_sampled_rows(D, causal):
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == 0
     rng = np.random.default_rng(43)
-    rows = sorted({0, 1, 127, 128, 16383, 16384, T - 129, T - 128, T - 2, T - 1} | set(rng.integers(0, T, 16).tolist()))
+    rows = sorted({0, 1, 127, 128, 16383, 16384, T // 2, T - 129, T - 128, T - 2, T - 1}
+                  | set(rng.integers(0, T, 16).tolist()))
     qf, kf, vf, df = (to_f64(t[0, 0]) for t in (q, k, v, do))
     o_ref, lse_ref = oracle.attn_fwd_rows(qf, kf, vf, scale, causal, rows)
     o_got = to_f64(o[0, 0].cpu())[rows]
